@@ -1,0 +1,143 @@
+/*
+ * m3_ssm.h -- C ABI of the Mamba-3 SSM layer core on NVIDIA B300 (sm_103a).
+ *
+ * What the library computes (paper: "Mamba-3: Improved Sequence Modeling
+ * using State Space Principles"):
+ *
+ *   For every batch row b and head h independently, over tokens t:
+ *     alpha_t = exp(dt_t A_h),  beta_t = (1 - lambda_t) dt_t alpha_t,
+ *     gamma_t = lambda_t dt_t                                   (Proposition 1)
+ *     phi_t   = phi_{t-1} + dt_t theta_t   (one angle per state pair (2k, 2k+1))
+ *     B~_t = R(phi_t)^T B_t,  C~_t = R(phi_t)^T C_t             (Proposition 3)
+ *     h_t = alpha_t h_{t-1} + beta_t B~_{t-1} X_{t-1}^T + gamma_t B~_t X_t^T
+ *                                      (Proposition 4; MIMO rank R, section 3.3)
+ *     y_t = h_t^T C~_t                                          (P x R)
+ *   with R(phi)^T (u, v) = (cos(phi) u + sin(phi) v, -sin(phi) u + cos(phi) v)
+ *   and B~_{t-1} the previous token's B rotated by its own angle phi_{t-1}.
+ *
+ * Layouts: row-major, innermost index last, densely packed, no strides.
+ *   x, y      [B][T][H][R][P]   (x[b,t,h,r,p] = X_t[p, r] of head h)
+ *   B, C      [B][T][H][R][N]   (B[b,t,h,r,n] = B_t[n, r])
+ *   dt,lambda [B][T][H]
+ *   theta     [B][T][H][N/2]
+ *   A         [H]                float32
+ *   state:  h [B][H][N][P] float32;  phi [B][H][N/2] float32;
+ *           prev_B [B][H][R][N], prev_x [B][H][R][P] in the input dtype
+ *           (the raw, unrotated previous token; phi is its angle).
+ * R = 1 is the SISO model; the R axis then has extent 1.
+ *
+ * Ownership: every pointer is device memory owned by the caller.  The
+ * library allocates no device memory.  All calls are asynchronous on the
+ * given stream (a cudaStream_t passed as void*; NULL = legacy default
+ * stream).  Argument errors are found on the host before anything is
+ * enqueued and are returned synchronously; nothing is launched then.
+ * Launch failures return M3_ERR_CUDA.  Errors found on the device (a bounded
+ * wait that ran out) are recorded in the workspace and read back with
+ * m3_ssm_device_status.
+ *
+ * All pointers must be 16-byte aligned (M3_ERR_ALIGN otherwise).
+ */
+#ifndef M3_SSM_H_
+#define M3_SSM_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  M3_OK = 0,
+  M3_ERR_ARG = 1,         /* null pointer where one is required, bad enum value */
+  M3_ERR_SHAPE = 2,       /* a size is negative, odd N, unsupported R, too large */
+  M3_ERR_DTYPE = 3,       /* dtype combination not supported */
+  M3_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned */
+  M3_ERR_CUDA = 5,        /* a CUDA launch or call failed */
+  M3_ERR_TIMEOUT = 6,     /* a device-side bounded wait ran out (see m3_ssm_device_status) */
+  M3_ERR_UNSUPPORTED = 7, /* valid request this build does not implement (e.g. chunk value) */
+  M3_ERR_WORKSPACE = 8    /* workspace missing or smaller than m3_ssm_prefill_workspace() */
+} m3_status;
+
+typedef enum { M3_F32 = 0, M3_BF16 = 1 } m3_dtype;
+
+typedef struct {
+  int B;              /* batch rows */
+  int T;              /* tokens (prefill); ignored by the decode step */
+  int H;              /* heads */
+  int P;              /* head dimension (multiple of 4, <= 256) */
+  int N;              /* state dimension (even, <= 256); N/2 rotation pairs */
+  int R;              /* MIMO rank: 1, 2, 4 or 8 (1 = SISO) */
+  int chunk;          /* prefill chunk length in tokens: 0 = the kernel's own choice.
+                         The result does not depend on it (the chunked form is the
+                         same linear map reassociated).  The bf16 tensor-core path
+                         runs 128/R tokens per chunk; any other nonzero value
+                         returns M3_ERR_UNSUPPORTED there. */
+  m3_dtype in_dtype;  /* x, B, C, dt, lambda, theta, prev_B, prev_x */
+  m3_dtype out_dtype; /* y */
+} m3_dims;
+
+typedef struct {
+  float* h;     /* [B][H][N][P] */
+  float* phi;   /* [B][H][N/2] */
+  void* prev_B; /* [B][H][R][N], in_dtype */
+  void* prev_x; /* [B][H][R][P], in_dtype */
+} m3_state;
+
+/*
+ * Bytes of device workspace m3_ssm_prefill needs for these dimensions
+ * (always >= 256).  The workspace must be zero-filled before its first use;
+ * the library leaves it ready for the next call afterwards.  One workspace
+ * may serve calls that are ordered on one stream, not calls that overlap.
+ */
+size_t m3_ssm_prefill_workspace(const m3_dims* dims);
+
+/*
+ * Chunked prefill over T tokens (paper section 2.3 and Eq. (7): the masked
+ * matrix form, decay mask times the 2-band convolution matrix; chunked as in
+ * section 3.3 "parallel within a chunk, recurrent across chunks").
+ *
+ *   h0   entry state, or NULL for a fresh sequence (h = 0, phi = 0, no previous
+ *        token).  Read only.
+ *   y    output [B][T][H][R][P] in out_dtype.
+ *   hT   exit state (h_T, phi_T, prev_B = B_{T-1}, prev_x = x_{T-1}), or NULL.
+ *        hT may alias h0 member by member (in-place continuation).  With
+ *        T = 0, hT receives a copy of h0 (or the zero state).
+ *   workspace / ws_bytes: caller-owned scratch, see m3_ssm_prefill_workspace.
+ *
+ * bf16 inputs with P = 64, N in {64, 128}, R in {1, 2, 4, 8} run on the
+ * tcgen05 tensor-core kernel; every other supported shape, and fp32 inputs,
+ * run on a CUDA-core recurrent kernel with fp32 arithmetic.
+ */
+m3_status m3_ssm_prefill(const m3_dims* dims, const void* x, const void* B, const void* C,
+                         const void* dt, const float* A, const void* lambda, const void* theta,
+                         const m3_state* h0, void* y, const m3_state* hT, void* workspace,
+                         size_t ws_bytes, void* stream);
+
+/*
+ * One decode step (the recurrence above for a single token; paper section
+ * 3.3 and Table 6's single-token decode).  `state` is read and updated in
+ * place: h <- h', phi <- phi + dt theta, prev_B <- B_t, prev_x <- x_t.
+ * Per-token inputs have the prefill layouts with T = 1:
+ *   x_t [B][H][R][P], B_t/C_t [B][H][R][N], dt_t/lambda_t [B][H], theta_t [B][H][N/2].
+ *   y_t [B][H][R][P] in out_dtype.
+ * dims->T and dims->chunk are ignored.  No workspace is used.
+ */
+m3_status m3_ssm_decode_step(const m3_dims* dims, const m3_state* state, const void* x_t,
+                             const void* B_t, const void* C_t, const void* dt_t, const float* A,
+                             const void* lambda_t, const void* theta_t, void* y_t, void* stream);
+
+/*
+ * Waits for `stream`, then reads and clears the device status word kept in
+ * `workspace`.  Returns M3_OK, M3_ERR_TIMEOUT (a bounded wait inside a
+ * prefill kernel ran out; that call's outputs are invalid), or M3_ERR_CUDA.
+ */
+m3_status m3_ssm_device_status(void* workspace, void* stream);
+
+/* Short English description of a status code (static storage). */
+const char* m3_status_str(m3_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* M3_SSM_H_ */

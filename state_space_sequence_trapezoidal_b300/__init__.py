@@ -1,0 +1,24 @@
+"""Mamba-3 SSM layer core on NVIDIA B300 (sm_103a).
+
+The computation lives in ``libm3ssm.so`` (CUDA; C ABI in ``include/m3_ssm.h``):
+a chunked tcgen05/TMA prefill, a CUDA-core recurrent prefill for fp32, and a
+bandwidth-bound decode step.  This package is the thin Python binding.
+"""
+from ._binding import (  # noqa: F401
+    M3_BF16,
+    M3_ERR_TIMEOUT,
+    M3_F32,
+    M3_OK,
+    M3Dims,
+    M3Error,
+    M3State,
+    State,
+    library_path,
+    load,
+    m3_ssm_decode_step,
+    m3_ssm_device_status,
+    m3_ssm_prefill,
+    m3_ssm_prefill_workspace,
+    status_str,
+    workspace_for,
+)

@@ -1,0 +1,205 @@
+"""ctypes binding of ``libm3ssm.so`` (declared in ``include/m3_ssm.h``).
+
+Argument marshalling only: torch supplies device memory and streams, and every
+step of the computation runs in the library's CUDA kernels.  There is no
+fallback: if the library cannot be loaded, or a call returns an error status,
+the functions here raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+from . import build as _build
+
+M3_OK = 0
+M3_ERR_TIMEOUT = 6
+M3_F32, M3_BF16 = 0, 1
+_DT = {torch.float32: M3_F32, torch.bfloat16: M3_BF16}
+
+
+class M3Dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in
+                ("B", "T", "H", "P", "N", "R", "chunk", "in_dtype", "out_dtype")]
+
+
+class M3State(ctypes.Structure):
+    _fields_ = [("h", ctypes.c_void_p), ("phi", ctypes.c_void_p), ("prev_B", ctypes.c_void_p),
+                ("prev_x", ctypes.c_void_p)]
+
+
+class M3Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: m3 status {status} ({status_str(status)})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load libm3ssm.so (building it first if the sources are newer)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if _build.needs_build():
+                _build.build()
+            lib = ctypes.CDLL(_build.LIB)
+            vp, sz = ctypes.c_void_p, ctypes.c_size_t
+            dp, sp = ctypes.POINTER(M3Dims), ctypes.POINTER(M3State)
+            lib.m3_ssm_prefill_workspace.argtypes = [dp]
+            lib.m3_ssm_prefill_workspace.restype = sz
+            lib.m3_ssm_prefill.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, sp, vp, sp, vp, sz, vp]
+            lib.m3_ssm_prefill.restype = ctypes.c_int
+            lib.m3_ssm_decode_step.argtypes = [dp, sp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+            lib.m3_ssm_decode_step.restype = ctypes.c_int
+            lib.m3_ssm_device_status.argtypes = [vp, vp]
+            lib.m3_ssm_device_status.restype = ctypes.c_int
+            lib.m3_status_str.argtypes = [ctypes.c_int]
+            lib.m3_status_str.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def status_str(status: int) -> str:
+    return load().m3_status_str(int(status)).decode()
+
+
+@dataclass
+class State:
+    """Recurrent state of the SSM core for B x H sequences.
+
+    h [B,H,N,P] float32; phi [B,H,N/2] float32 (cumulative angle of the last
+    token, kept reduced to [-pi, pi]); prev_B [B,H,R,N] and prev_x [B,H,R,P]
+    in the input dtype (the last token's raw B and x).
+    """
+
+    h: torch.Tensor
+    phi: torch.Tensor
+    prev_B: torch.Tensor
+    prev_x: torch.Tensor
+
+    @staticmethod
+    def zeros(B, H, N, P, R=1, dtype=torch.bfloat16, device="cuda") -> "State":
+        return State(torch.zeros(B, H, N, P, dtype=torch.float32, device=device),
+                     torch.zeros(B, H, N // 2, dtype=torch.float32, device=device),
+                     torch.zeros(B, H, R, N, dtype=dtype, device=device),
+                     torch.zeros(B, H, R, P, dtype=dtype, device=device))
+
+    def clone(self) -> "State":
+        return State(self.h.clone(), self.phi.clone(), self.prev_B.clone(), self.prev_x.clone())
+
+    def _c(self) -> M3State:
+        for t in (self.h, self.phi, self.prev_B, self.prev_x):
+            if not t.is_contiguous():
+                raise ValueError("state tensors must be contiguous")
+        return M3State(self.h.data_ptr(), self.phi.data_ptr(), self.prev_B.data_ptr(),
+                       self.prev_x.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_inputs(ts, dtype):
+    dev = None
+    for name, t in ts.items():
+        if t.dtype != dtype:
+            raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+        if not t.is_cuda:
+            raise ValueError(f"{name}: must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name}: must be contiguous")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"{name}: on {t.device}, others on {dev}")
+    return dev
+
+
+def _dims(x, dt, theta, chunk, in_dt, out_dt, prefill=True) -> M3Dims:
+    if prefill:
+        Bsz, T, H = dt.shape
+    else:
+        (Bsz, H), T = dt.shape, 0
+    N = theta.shape[-1] * 2
+    P = x.shape[-1]
+    R = x.shape[-2] if x.dim() == (5 if prefill else 4) else 1
+    return M3Dims(Bsz, T, H, P, N, R, chunk, _DT[in_dt], _DT[out_dt])
+
+
+def m3_ssm_prefill_workspace(dims: M3Dims) -> int:
+    return int(load().m3_ssm_prefill_workspace(ctypes.byref(dims)))
+
+
+def workspace_for(dims: M3Dims, device) -> torch.Tensor:
+    """A zero-filled workspace tensor for m3_ssm_prefill."""
+    n = m3_ssm_prefill_workspace(dims)
+    return torch.zeros((n + 15) // 16 * 16, dtype=torch.uint8, device=device)
+
+
+def m3_ssm_prefill(x, B, C, dt, A, lam, theta, h0: State | None = None, *, y=None,
+                   hT: State | None = None, workspace=None, chunk: int = 0,
+                   out_dtype=torch.float32, stream=None):
+    """Chunked prefill.  x [B,T,H,R,P] (or [B,T,H,P] for R = 1), B/C [B,T,H,R,N]
+    (or [B,T,H,N]), dt/lam [B,T,H], A [H] float32, theta [B,T,H,N/2].
+    Returns y [B,T,H,R,P] in ``out_dtype`` (or writes the given ``y``).
+    ``hT`` (optional) receives the exit state; it may be ``h0`` itself."""
+    in_dt = x.dtype
+    dev = _check_inputs(dict(x=x, B=B, C=C, dt=dt, lam=lam, theta=theta), in_dt)
+    _check_inputs(dict(A=A), torch.float32)
+    d = _dims(x, dt, theta, chunk, in_dt, out_dtype)
+    if y is None:
+        y = torch.empty(d.B, d.T, d.H, d.R, d.P, dtype=out_dtype, device=dev)
+    elif y.dtype != out_dtype or not y.is_contiguous() or y.numel() != d.B * d.T * d.H * d.R * d.P:
+        raise ValueError("y: wrong dtype, layout or size")
+    if workspace is None:
+        workspace = workspace_for(d, dev)
+    c0 = h0._c() if h0 is not None else None
+    c1 = hT._c() if hT is not None else None
+    st = load().m3_ssm_prefill(ctypes.byref(d), x.data_ptr(), B.data_ptr(), C.data_ptr(),
+                               dt.data_ptr(), A.data_ptr(), lam.data_ptr(), theta.data_ptr(),
+                               ctypes.byref(c0) if c0 is not None else None, y.data_ptr(),
+                               ctypes.byref(c1) if c1 is not None else None,
+                               workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    if st != M3_OK:
+        raise M3Error(st, "m3_ssm_prefill")
+    return y
+
+
+def m3_ssm_decode_step(state: State, x_t, B_t, C_t, dt_t, A, lam_t, theta_t, *, y_t=None,
+                       out_dtype=torch.float32, stream=None):
+    """One decode step, updating ``state`` in place.  x_t [B,H,R,P] (or [B,H,P]),
+    B_t/C_t [B,H,R,N] (or [B,H,N]), dt_t/lam_t [B,H], theta_t [B,H,N/2].
+    Returns y_t [B,H,R,P] in ``out_dtype``."""
+    in_dt = x_t.dtype
+    dev = _check_inputs(dict(x_t=x_t, B_t=B_t, C_t=C_t, dt_t=dt_t, lam_t=lam_t, theta_t=theta_t),
+                        in_dt)
+    _check_inputs(dict(A=A), torch.float32)
+    d = _dims(x_t, dt_t, theta_t, 0, in_dt, out_dtype, prefill=False)
+    if y_t is None:
+        y_t = torch.empty(d.B, d.H, d.R, d.P, dtype=out_dtype, device=dev)
+    c = state._c()
+    st = load().m3_ssm_decode_step(ctypes.byref(d), ctypes.byref(c), x_t.data_ptr(),
+                                   B_t.data_ptr(), C_t.data_ptr(), dt_t.data_ptr(), A.data_ptr(),
+                                   lam_t.data_ptr(), theta_t.data_ptr(), y_t.data_ptr(),
+                                   _stream_handle(stream))
+    if st != M3_OK:
+        raise M3Error(st, "m3_ssm_decode_step")
+    return y_t
+
+
+def m3_ssm_device_status(workspace: torch.Tensor, stream=None) -> int:
+    """Status word of a prefill workspace (waits for the stream): M3_OK or M3_ERR_TIMEOUT."""
+    return int(load().m3_ssm_device_status(workspace.data_ptr(), _stream_handle(stream)))

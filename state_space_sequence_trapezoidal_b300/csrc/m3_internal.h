@@ -1,0 +1,51 @@
+// Internal interface between the C-ABI layer (m3_api.cu) and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "m3_ssm.h"
+
+namespace m3 {
+
+// Validated arguments of one prefill call.  State pointers are null when the
+// caller passed no entry state (fresh sequence) or wants no exit state.
+struct PrefillArgs {
+  m3_dims d;
+  const void* x;
+  const void* B;
+  const void* C;
+  const void* dt;
+  const float* A;
+  const void* lam;
+  const void* theta;
+  m3_state h0;  // all members null for a fresh sequence
+  void* y;
+  m3_state hT;  // all members null when no exit state is wanted
+  unsigned* status;  // device status word (first bytes of the workspace)
+};
+
+struct DecodeArgs {
+  m3_dims d;
+  m3_state s;
+  const void* x;
+  const void* B;
+  const void* C;
+  const void* dt;
+  const float* A;
+  const void* lam;
+  const void* theta;
+  void* y;
+};
+
+// Tensor-core (tcgen05) chunked prefill: bf16 inputs, P = 64, N in {64, 128}, R in {1,2,4,8}.
+bool prefill_tc_supported(const m3_dims& d);
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
+
+// CUDA-core recurrent prefill (fp32 arithmetic): every shape the API accepts.
+bool prefill_recurrent_supported(const m3_dims& d);
+cudaError_t launch_prefill_recurrent(const PrefillArgs& a, cudaStream_t s);
+
+bool decode_supported(const m3_dims& d);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+}  // namespace m3

@@ -1,0 +1,101 @@
+"""The C-ABI library loads, exports every function include/m3_ssm.h declares, and
+rejects bad arguments on the host before anything reaches a GPU.
+
+None of these calls launches a kernel: each one fails validation first."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import state_space_sequence_trapezoidal_b300 as m3
+from state_space_sequence_trapezoidal_b300 import M3Dims, M3State
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+OK, ARG, SHAPE, DTYPE, ALIGN, CUDA, TIMEOUT, UNSUP, WS = range(9)
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(m3_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported():
+    lib = m3.load()
+    names = declared_functions()
+    assert {"m3_ssm_prefill", "m3_ssm_decode_step", "m3_ssm_prefill_workspace",
+            "m3_ssm_device_status", "m3_status_str"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported by libm3ssm.so"
+
+
+def test_status_strings():
+    lib = m3.load()
+    for s in range(9):
+        assert lib.m3_status_str(s)
+    assert lib.m3_status_str(99) == b"unknown status"
+
+
+def _dims(**kw):
+    d = dict(B=2, T=8, H=3, P=64, N=128, R=1, chunk=0, in_dtype=1, out_dtype=0)
+    d.update(kw)
+    return M3Dims(**d)
+
+
+def _prefill(d, ptrs=None, ws=256, h0=None, hT=None):
+    lib = m3.load()
+    p = dict(x=16, B=16, C=16, dt=16, A=16, lam=16, theta=16, y=16, ws=16)
+    p.update(ptrs or {})
+    return lib.m3_ssm_prefill(ctypes.byref(d) if d is not None else None, p["x"], p["B"], p["C"],
+                              p["dt"], p["A"], p["lam"], p["theta"],
+                              ctypes.byref(h0) if h0 else None, p["y"],
+                              ctypes.byref(hT) if hT else None, p["ws"], ws, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(N=127), SHAPE), (dict(N=0), SHAPE), (dict(N=258), SHAPE), (dict(P=6), SHAPE),
+    (dict(P=0), SHAPE), (dict(R=3), SHAPE), (dict(B=-1), SHAPE), (dict(T=-1), SHAPE),
+    (dict(chunk=-1), SHAPE), (dict(in_dtype=7), DTYPE), (dict(out_dtype=5), DTYPE),
+    (dict(chunk=64), UNSUP),
+])
+def test_prefill_rejects_bad_dims(kw, code):
+    assert _prefill(_dims(**kw)) == code
+
+
+def test_prefill_rejects_null_and_misaligned_pointers():
+    assert _prefill(None) == ARG
+    assert _prefill(_dims(), dict(x=None)) == ARG
+    assert _prefill(_dims(), dict(A=None)) == ARG
+    assert _prefill(_dims(), dict(ws=None)) == WS
+    assert _prefill(_dims(), ws=8) == WS
+    assert _prefill(_dims(), dict(theta=24)) == ALIGN
+    assert _prefill(_dims(), dict(y=4)) == ALIGN
+    partial = M3State(16, None, 16, 16)
+    assert _prefill(_dims(), h0=partial) == ARG
+    assert _prefill(_dims(), hT=M3State(16, 16, 16, 8)) == ALIGN
+
+
+def test_workspace_size():
+    assert m3.m3_ssm_prefill_workspace(_dims()) >= 256
+
+
+def test_decode_rejects_bad_arguments():
+    lib = m3.load()
+    st = M3State(16, 16, 16, 16)
+
+    def call(d, state=st, x=16):
+        return lib.m3_ssm_decode_step(ctypes.byref(d), ctypes.byref(state) if state else None,
+                                      x, 16, 16, 16, 16, 16, 16, 16, None)
+
+    assert call(_dims(N=5)) == SHAPE
+    assert call(_dims(R=5)) == SHAPE
+    assert call(_dims(), state=None) == ARG
+    assert call(_dims(), x=None) == ARG
+    assert call(_dims(), x=40) == ALIGN
+    assert call(_dims(), state=M3State(16, 16, None, 16)) == ARG

@@ -1,0 +1,280 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the fp64 oracle.
+
+Element-by-element comparisons on seeded inputs at sizes the oracle finishes in
+seconds (several chunks plus a ragged tail, random entry states that exercise the
+previous-token fold), and sampled (b, h) sequences at the full benchmark sizes in
+the benchmark's launch configuration.  The error measure is max|gpu - oracle| over
+the compared elements divided by their RMS: <= 1e-4 for fp32 inputs, <= 2e-2 for
+bf16 inputs with fp32 accumulation.
+"""
+import numpy as np
+import pytest
+import torch
+
+import state_space_sequence_trapezoidal_b300 as m3
+from state_space_sequence_trapezoidal_b300 import synth
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+
+def prefill_gpu(inp_dev, h0=None, out_dtype=torch.float32, want_state=True, chunk=0):
+    x = inp_dev["x"]
+    Bsz, T, H, R, Pd = x.shape
+    N = inp_dev["B"].shape[-1]
+    hT = m3.State.zeros(Bsz, H, N, Pd, R, dtype=x.dtype) if want_state else None
+    ws = m3.workspace_for(m3.M3Dims(Bsz, T, H, Pd, N, R, 0, 0, 0), x.device)
+    y = m3.m3_ssm_prefill(inp_dev["x"], inp_dev["B"], inp_dev["C"], inp_dev["dt"], inp_dev["A"],
+                          inp_dev["lambda"], inp_dev["theta"], h0, hT=hT, workspace=ws,
+                          out_dtype=out_dtype, chunk=chunk)
+    torch.cuda.synchronize()
+    assert m3.m3_ssm_device_status(ws) == m3.M3_OK
+    return y, hT
+
+
+# ------------------------------------------------------------------ small, full comparison
+
+
+def test_tiny_siso_f32_workload():
+    """The tiny fp32 SISO check (B1 H2 T256 P16 N16, zero initial state), every element."""
+    w = synth.WORKLOADS["tiny-siso-f32-b1-h2-t256-p16-n16"]
+    inp = synth.make_inputs(w.B, w.T, w.H, w.P, w.N, w.R, w.seed, w.dtype)
+    y, hT = prefill_gpu(P.to_device(inp, "f32"))
+    sl = P.all_slices(w.B, w.H)
+    yr, sr = P.run_oracle(inp, sl)
+    e = P.rel_err(P.pick(y.cpu().numpy(), sl, True), yr)
+    assert e <= P.TOL["f32"], e
+    P.check_state({k: P.pick(v, sl, False) for k, v in P.state_to_host(hT).items()}, sr, "f32")
+
+
+@pytest.mark.parametrize("N,Pd,R,T", [(6, 8, 2, 37), (16, 16, 1, 1), (32, 12, 4, 70), (128, 64, 1, 150),
+                                      (64, 64, 4, 33)])
+def test_f32_recurrent_shapes_with_entry_state(N, Pd, R, T):
+    B, H = 2, 3
+    inp = synth.make_inputs(B, T, H, Pd, N, R, 11 + N + T, "f32")
+    st0 = P.random_state(B, H, N, Pd, R, "f32", 5)
+    y, hT = prefill_gpu(P.to_device(inp, "f32"), P.state_to_device(st0, "f32"))
+    sl = P.all_slices(B, H)
+    yr, sr = P.run_oracle(inp, sl, st0)
+    assert P.rel_err(P.pick(y.cpu().numpy(), sl, True), yr) <= P.TOL["f32"]
+    P.check_state({k: P.pick(v, sl, False) for k, v in P.state_to_host(hT).items()}, sr, "f32")
+
+
+TC_SHAPES = [(128, 1), (128, 2), (128, 4), (128, 8), (64, 1), (64, 2), (64, 4), (64, 8)]
+
+
+@pytest.mark.parametrize("N,R", TC_SHAPES)
+@pytest.mark.parametrize("fresh", [False, True])
+def test_bf16_tensor_core_prefill(N, R, fresh):
+    """tcgen05 path: three full chunks plus a ragged tail, entry state folded in."""
+    B, H, Pd = 2, 3, 64
+    CT = 128 // R
+    T = 3 * CT + CT // 2 + 3
+    inp = synth.make_inputs(B, T, H, Pd, N, R, 1000 + N + R, "bf16")
+    st0 = None if fresh else P.random_state(B, H, N, Pd, R, "bf16", 7)
+    y, hT = prefill_gpu(P.to_device(inp, "bf16"),
+                        None if fresh else P.state_to_device(st0, "bf16"))
+    sl = P.all_slices(B, H)
+    yr, sr = P.run_oracle(inp, sl, st0)
+    e = P.rel_err(P.pick(y.cpu().numpy(), sl, True), yr)
+    assert e <= P.TOL["bf16"], e
+    P.check_state({k: P.pick(v, sl, False) for k, v in P.state_to_host(hT).items()}, sr, "bf16")
+
+
+@pytest.mark.parametrize("N,R", [(128, 1), (64, 4)])
+def test_bf16_output_dtype(N, R):
+    """y rounded to bf16: bound = the fp32-output tolerance plus one bf16 rounding (2^-8 |y|)."""
+    B, H, Pd, T = 2, 2, 64, 200
+    inp = synth.make_inputs(B, T, H, Pd, N, R, 77, "bf16")
+    y, _ = prefill_gpu(P.to_device(inp, "bf16"), out_dtype=torch.bfloat16)
+    sl = P.all_slices(B, H)
+    yr, _ = P.run_oracle(inp, sl)
+    got = P.pick(y.float().cpu().numpy(), sl, True)
+    rms = np.sqrt(np.mean(yr * yr))
+    assert np.all(np.abs(got - yr) <= P.TOL["bf16"] * rms + 2.0 ** -8 * np.abs(yr))
+
+
+@pytest.mark.parametrize("N,R,dtype", [(128, 1, "bf16"), (64, 4, "bf16"), (16, 1, "f32")])
+def test_continuation_across_calls(N, R, dtype):
+    """prefill(0:T1) -> state -> prefill(T1:T) matches prefill(0:T) and the oracle; the exit
+    state is written over the entry state (in-place continuation)."""
+    B, H, Pd, T = 2, 2, (64 if dtype == "bf16" else 16), 300
+    inp = synth.make_inputs(B, T, H, Pd, N, R, 99, dtype)
+    dev = P.to_device(inp, dtype)
+    y_full, st_full = prefill_gpu(dev)
+    T1 = 131
+    a = {k: (v[:, :T1].contiguous() if k != "A" else v) for k, v in dev.items()}
+    b = {k: (v[:, T1:].contiguous() if k != "A" else v) for k, v in dev.items()}
+    y1, st = prefill_gpu(a)
+    ws = m3.workspace_for(m3.M3Dims(), st.h.device)
+    y2 = m3.m3_ssm_prefill(b["x"], b["B"], b["C"], b["dt"], b["A"], b["lambda"], b["theta"], st,
+                           hT=st, workspace=ws)
+    torch.cuda.synchronize()
+    y_split = torch.cat([y1, y2], 1).cpu().numpy()
+    sl = P.all_slices(B, H)
+    yr, sr = P.run_oracle(inp, sl)
+    assert P.rel_err(P.pick(y_split, sl, True), yr) <= P.TOL[dtype]
+    assert P.rel_err(P.pick(y_full.cpu().numpy(), sl, True), yr) <= P.TOL[dtype]
+    P.check_state({k: P.pick(v, sl, False) for k, v in P.state_to_host(st).items()}, sr, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_zero_tokens_copies_state(dtype):
+    B, H, N, Pd, R = 2, 2, 64, 64, 4
+    inp = synth.make_inputs(B, 0, H, Pd, N, R, 1, dtype)
+    st0 = P.random_state(B, H, N, Pd, R, dtype, 3)
+    y, hT = prefill_gpu(P.to_device(inp, dtype), P.state_to_device(st0, dtype))
+    assert y.numel() == 0
+    got = P.state_to_host(hT)
+    np.testing.assert_array_equal(got["h"], st0["h"])
+    np.testing.assert_array_equal(got["prev_B"], st0["prev_B"])
+    assert P.phi_err(got["phi"], st0["phi"]) < 1e-6
+
+
+def test_empty_batch_is_a_noop():
+    inp = synth.make_inputs(0, 10, 3, 64, 128, 1, 1, "bf16")
+    y, _ = prefill_gpu(P.to_device(inp, "bf16"), want_state=False)
+    assert y.shape[0] == 0
+
+
+def test_chunk_argument():
+    """chunk = 128/R selects the tensor-core kernel's own length; other values are refused."""
+    inp = P.to_device(synth.make_inputs(1, 40, 2, 64, 128, 1, 5, "bf16"), "bf16")
+    y0, _ = prefill_gpu(inp)
+    y1, _ = prefill_gpu(inp, chunk=128)
+    assert torch.equal(y0, y1)
+    with pytest.raises(m3.M3Error):
+        prefill_gpu(inp, chunk=64)
+
+
+@pytest.mark.parametrize("N,R", [(128, 1), (64, 4)])
+def test_rerun_is_bit_identical(N, R):
+    inp = P.to_device(synth.make_inputs(2, 500, 4, 64, N, R, 8, "bf16"), "bf16")
+    y1, s1 = prefill_gpu(inp)
+    y2, s2 = prefill_gpu(inp)
+    assert torch.equal(y1, y2) and torch.equal(s1.h, s2.h)
+
+
+# ------------------------------------------------------------------ decode
+
+
+def decode_inputs(B, H, Pd, N, R, dtype, base_seed, step):
+    i = synth.make_inputs(B, 1, H, Pd, N, R, synth.decode_step_seed(base_seed, step), dtype,
+                          A_seed=base_seed)
+    return {k: (v[:, 0] if k != "A" else v) for k, v in i.items()}
+
+
+@pytest.mark.parametrize("N,Pd,R,dtype", [(128, 64, 1, "bf16"), (64, 64, 4, "bf16"), (16, 16, 1, "f32"),
+                                          (6, 8, 2, "f32"), (32, 12, 8, "bf16")])
+def test_decode_steps_match_oracle(N, Pd, R, dtype):
+    B, H, K = 3, 5, 6
+    st0 = P.random_state(B, H, N, Pd, R, dtype, 21)
+    state = P.state_to_device(st0, dtype)
+    ref_state = {k: v.copy() for k, v in st0.items()}
+    sl = P.all_slices(B, H)
+    ref_state = {k: P.pick(v, sl, False) for k, v in ref_state.items()}
+    for s in range(K):
+        inp = decode_inputs(B, H, Pd, N, R, dtype, 500, s)
+        dev = P.to_device(inp, dtype)
+        y = m3.m3_ssm_decode_step(state, dev["x"], dev["B"], dev["C"], dev["dt"], dev["A"],
+                                  dev["lambda"], dev["theta"])
+        torch.cuda.synchronize()
+        seq = {k: (v[:, None] if k != "A" else v) for k, v in inp.items()}  # T = 1
+        yr, ref_state = P.run_oracle(seq, sl, {k: _unpick(v, sl, B, H) for k, v in ref_state.items()})
+        e = P.rel_err(P.pick(y.cpu().numpy(), sl, False), yr[:, 0])
+        assert e <= P.TOL[dtype], (s, e)
+    P.check_state({k: P.pick(v, sl, False) for k, v in P.state_to_host(state).items()}, ref_state,
+                  dtype)
+
+
+def _unpick(stack, slices, B, H):
+    out = np.zeros((B, H) + stack.shape[1:], stack.dtype)
+    for i, (b, h) in enumerate(slices):
+        out[b, h] = stack[i]
+    return out
+
+
+@pytest.mark.parametrize("N,R", [(128, 1), (64, 4)])
+def test_prefill_equals_decode_loop(N, R):
+    """The chunked prefill and a loop of decode steps compute the same recurrence."""
+    B, H, Pd, T = 2, 3, 64, 45
+    inp = synth.make_inputs(B, T, H, Pd, N, R, 31, "bf16")
+    st0 = P.random_state(B, H, N, Pd, R, "bf16", 4)
+    dev = P.to_device(inp, "bf16")
+    y_pf, st_pf = prefill_gpu(dev, P.state_to_device(st0, "bf16"))
+    state = P.state_to_device(st0, "bf16")
+    ys = []
+    for t in range(T):
+        ys.append(m3.m3_ssm_decode_step(state, dev["x"][:, t].contiguous(), dev["B"][:, t].contiguous(),
+                                        dev["C"][:, t].contiguous(), dev["dt"][:, t].contiguous(),
+                                        dev["A"], dev["lambda"][:, t].contiguous(),
+                                        dev["theta"][:, t].contiguous()))
+    y_dec = torch.stack(ys, 1)
+    torch.cuda.synchronize()
+    a, b = y_pf.cpu().numpy(), y_dec.cpu().numpy()
+    assert P.rel_err(a, b) <= P.TOL["bf16"]
+    assert P.rel_err(st_pf.h.cpu().numpy(), state.h.cpu().numpy()) <= P.TOL["bf16"]
+
+
+# ------------------------------------------------------------------ full benchmark sizes
+
+
+@pytest.mark.parametrize("name", ["siso-prefill-bf16-b8-t4096-h32-p64-n128",
+                                  "mimo-r4-prefill-bf16-b8-t4096-h32-p64-n64"])
+def test_full_size_prefill_sampled(name):
+    w = synth.WORKLOADS[name]
+    inp = synth.make_inputs(w.B, w.T, w.H, w.P, w.N, w.R, w.seed, w.dtype)
+    y, hT = prefill_gpu(P.to_device(inp, w.dtype))
+    sl = P.sample_slices(w.B, w.H, 8, w.seed)
+    yr, sr = P.run_oracle(inp, sl)
+    e = P.rel_err(P.pick(y.cpu().numpy(), sl, True), yr)
+    assert e <= P.TOL[w.dtype], e
+    P.check_state({k: P.pick(v, sl, False) for k, v in P.state_to_host(hT).items()}, sr, w.dtype)
+
+
+def test_full_size_long_prefill_then_decode_sampled():
+    """B1 T16384 H32 SISO prefill, then 256 decode steps; 6 sampled heads against the oracle."""
+    w = synth.WORKLOADS["long-siso-prefill-bf16-b1-t16384-h32-p64-n128"]
+    inp = synth.make_inputs(w.B, w.T, w.H, w.P, w.N, w.R, w.seed, w.dtype)
+    y, st = prefill_gpu(P.to_device(inp, w.dtype))
+    sl = P.sample_slices(w.B, w.H, 6, w.seed)
+    yr, sr = P.run_oracle(inp, sl)
+    assert P.rel_err(P.pick(y.cpu().numpy(), sl, True), yr) <= P.TOL["bf16"]
+    dec = synth.make_inputs(w.B, w.decode_steps, w.H, w.P, w.N, w.R, w.seed + 100, w.dtype,
+                            A_seed=w.seed)
+    dd = P.to_device(dec, w.dtype)
+    ys = []
+    for s in range(w.decode_steps):
+        ys.append(m3.m3_ssm_decode_step(st, dd["x"][:, s].contiguous(), dd["B"][:, s].contiguous(),
+                                        dd["C"][:, s].contiguous(), dd["dt"][:, s].contiguous(),
+                                        dd["A"], dd["lambda"][:, s].contiguous(),
+                                        dd["theta"][:, s].contiguous()))
+    torch.cuda.synchronize()
+    y_dec = torch.stack(ys, 1).cpu().numpy()
+    yr2, sr2 = P.run_oracle(dec, sl, {k: _unpick(v, sl, w.B, w.H) for k, v in sr.items()})
+    assert P.rel_err(P.pick(y_dec, sl, True), yr2) <= P.TOL["bf16"]
+    P.check_state({k: P.pick(v, sl, False) for k, v in P.state_to_host(st).items()}, sr2, "bf16")
+
+
+@pytest.mark.parametrize("name", ["siso-decode-bf16-b256-h32-p64-n128",
+                                  "mimo-r4-decode-bf16-b256-h32-p64-n64"])
+def test_full_size_decode_sampled(name):
+    """B256 H32 decode from a 512-token prefill state, 16 steps at the full batch."""
+    w = synth.WORKLOADS[name]
+    pre = synth.make_inputs(w.B, w.prefill_T_for_decode, w.H, w.P, w.N, w.R, w.seed, w.dtype)
+    _, st = prefill_gpu(P.to_device(pre, w.dtype))
+    sl = P.sample_slices(w.B, w.H, 8, w.seed)
+    _, sr = P.run_oracle(pre, sl)
+    ref = {k: _unpick(v, sl, w.B, w.H) for k, v in sr.items()}
+    steps = 16
+    for s in range(steps):
+        inp = decode_inputs(w.B, w.H, w.P, w.N, w.R, w.dtype, w.seed, s)
+        dev = P.to_device(inp, w.dtype)
+        y = m3.m3_ssm_decode_step(st, dev["x"], dev["B"], dev["C"], dev["dt"], dev["A"],
+                                  dev["lambda"], dev["theta"])
+        seq = {k: (v[:, None] if k != "A" else v) for k, v in inp.items()}
+        yr, sr = P.run_oracle(seq, sl, ref)
+        ref = {k: _unpick(v, sl, w.B, w.H) for k, v in sr.items()}
+    torch.cuda.synchronize()
+    assert P.rel_err(P.pick(y.cpu().numpy(), sl, False), yr[:, 0]) <= P.TOL["bf16"]
+    P.check_state({k: P.pick(v, sl, False) for k, v in P.state_to_host(st).items()}, sr, "bf16")
