@@ -1,0 +1,483 @@
+#!/usr/bin/env python
+"""Benchmark of the Mamba-3 SSM layer core on B300: prefill and decode tokens/s, % of roofline.
+
+Headline (``value``): prefill tokens/s of the SISO 1.5B-layer workload
+(B 8, T 4096, H 32, P 64, N 128, bf16 inputs, fp32 accumulation and output),
+inputs resident in HBM.  The same line carries the dominant kernel's roofline,
+the fp64 CPU oracle's throughput on a bounded sample, an end-to-end number
+through the C ABI with host buffers, the decode legs (B 256 x H 32, 1000
+steps from a 512-token prefill state; SISO N 128 and MIMO R 4 N 64), the
+16384-token prefill + 256 decode steps, SM clocks during the timed regions,
+and the count of library kernel launches.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Several GPUs run independent replicas (torchrun, one rank per GPU): each rank
+draws its own inputs; a barrier and a max over ranks bracket the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Mamba-3 SSM prefill tokens/s & decode tokens/s, % of B300 roofline"
+HEADLINE = "siso-prefill-bf16-b8-t4096-h32-p64-n128"
+SISO_DEC = "siso-decode-bf16-b256-h32-p64-n128"
+MIMO_DEC = "mimo-r4-decode-bf16-b256-h32-p64-n64"
+MIMO_PRE = "mimo-r4-prefill-bf16-b8-t4096-h32-p64-n64"
+LONG = "long-siso-prefill-bf16-b1-t16384-h32-p64-n128"
+L2_BYTES = 126 * 1024 * 1024
+CHUNK_ROWS = 128  # (token, rank) rows per chunk of the tensor-core prefill
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+# ------------------------------------------------------------------ algorithmic counts
+
+
+def prefill_bytes(w, out_bytes=4) -> int:
+    """Mandatory HBM traffic of one prefill call from a fresh state, returning h_T."""
+    tok = w.B * w.T * w.H
+    inp = tok * (w.R * w.P * 2 + 2 * w.R * w.N * 2 + 2 * 2 + (w.N // 2) * 2)
+    out = tok * w.R * w.P * out_bytes
+    state = w.B * w.H * (w.N * w.P * 4 + (w.N // 2) * 4 + w.R * w.N * 2 + w.R * w.P * 2)
+    return inp + out + state + w.H * 4
+
+
+def prefill_flops(w, rows=CHUNK_ROWS) -> int:
+    """Flops of the chunked masked form at the kernel's chunk (full rows x rows score tiles)."""
+    c_tok = rows // w.R
+    per_chunk = 2 * rows * rows * w.N + 2 * rows * rows * w.P + 4 * rows * w.N * w.P
+    return w.B * w.H * per_chunk * (-(-w.T // c_tok))
+
+
+def decode_bytes(w, out_bytes=4) -> int:
+    """Mandatory HBM traffic of one decode step: state read + write, token inputs, y."""
+    bh = w.B * w.H
+    state = 2 * bh * (w.N * w.P * 4 + (w.N // 2) * 4 + w.R * w.N * 2 + w.R * w.P * 2)
+    inp = bh * (w.R * w.P * 2 + 2 * w.R * w.N * 2 + 2 * 2 + (w.N // 2) * 2)
+    return state + inp + bh * w.R * w.P * out_bytes + w.H * 4
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons; keeps samples inside marked windows."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.windows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                self.samples.append((time.time(), float(parts[0]), float(parts[1]), parts[3:7]))
+            except ValueError:
+                pass
+
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def summary(self):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        inside = [s for s in self.samples
+                  if any(a - 0.05 <= s[0] <= b + 0.05 for a, b in self.windows)]
+        use = inside or self.samples
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for s in use for n, v in zip(names, s[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(s[1] for s in use),
+                "sm_max_mhz": max(s[2] for s in use), "reasons": reasons, "samples": len(use),
+                "in_timed_regions": bool(inside)}
+
+
+# ------------------------------------------------------------------ helpers
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("m3_prefill_tc.cu", "m3_ptx.cuh"):
+        with open(os.path.join(ROOT, "state_space_sequence_trapezoidal_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, sha: str):
+    """Per-launch DRAM bytes from a committed ncu summary, only if taken on this kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e or e.get("source_sha") != sha:
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def gen_inputs_parallel(w, seeds, A_seed, dtype="bf16"):
+    """Per-step decode inputs, drawn in host threads (one seeded generator per step)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    from state_space_sequence_trapezoidal_b300 import synth
+
+    def one(s):
+        return synth.make_inputs(w.B, 1, w.H, w.P, w.N, w.R, s, dtype, A_seed=A_seed)
+
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4)) as ex:
+        return list(ex.map(one, seeds))
+
+
+def to_dev(inp, dev, torch):
+    return {k: torch.from_numpy(np.ascontiguousarray(v)).to(
+        dev, torch.float32 if k == "A" else torch.bfloat16) for k, v in inp.items()}
+
+
+# ------------------------------------------------------------------ the oracle arm
+
+
+def oracle_throughput(w, inp, budget_s: float, start: int = 0, min_slices: int = 0):
+    """Time the fp64 CPU oracle on whole (b, h) sequences of workload ``w`` (inputs ``inp``),
+    taking distinct sequences from index ``start`` on, in batches over all host cores, until
+    ``budget_s`` seconds of oracle time (and at least ``min_slices`` sequences).
+    Returns (tokens/s, threads used, sequences done, seconds)."""
+    import oracle
+
+    ncores = os.cpu_count() or 1
+    batch = max(8, ncores)
+    total = w.B * w.H
+    done, spent, used = 0, 0.0, 1
+    while (spent < budget_s or done < min_slices) and done < total:
+        ids = [(start + done + i) % total for i in range(min(batch, total - done))]
+        sl = [(i // w.H, i % w.H) for i in ids]
+        g = oracle.gather(inp, sl)
+        t0 = time.perf_counter()
+        _, _, used = oracle.scan(g["x"], g["Bm"], g["Cm"], g["dt"], g["A"], g["lam"], g["theta"])
+        spent += time.perf_counter() - t0
+        done += len(sl)
+    tokens = done * w.T / w.H  # a token carries all H heads
+    return tokens / spent, used, done, spent
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step is a bounded sample (a batch of whole
+    sequences) of the headline workload, timed on the host cores."""
+    from state_space_sequence_trapezoidal_b300 import dist as D
+    from state_space_sequence_trapezoidal_b300 import synth
+
+    rank, world, _ = D.env_rank()
+    if rank != 0:
+        return 0
+    w = synth.WORKLOADS[HEADLINE]
+    inp = synth.make_inputs(w.B, w.T, w.H, w.P, w.N, w.R, w.seed, w.dtype)
+    n_per_step = max(8, os.cpu_count() or 1)
+    tok, sec, used, pos = 0.0, 0.0, 1, 0
+    for i in range(args.warmup + args.steps):
+        _, used, done, spent = oracle_throughput(w, inp, budget_s=0.0, start=pos,
+                                                 min_slices=n_per_step)
+        pos += done
+        if i >= args.warmup:
+            tok += done * w.T / w.H
+            sec += spent
+    value = tok / sec
+    desc = (f"each step: {n_per_step} whole (b,h) sequences x {w.T} tokens of {w.name} "
+            f"(fp64, OpenMP over sequences); tokens counted as sequences x T / H")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "P": w.P, "N": w.N, "R": w.R},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--decode-steps", type=int, default=1000)
+    ap.add_argument("--skip-extras", action="store_true", help="headline prefill only")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+
+    import state_space_sequence_trapezoidal_b300 as m3
+    from state_space_sequence_trapezoidal_b300 import dist as D
+    from state_space_sequence_trapezoidal_b300 import synth
+
+    rank, world, local = D.init("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    m3.load()
+    peaks = load_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    clocks = ClockSampler(f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local))
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn, n):
+        """Run fn n times between two events on the launching stream; returns ms per call."""
+        D.barrier()
+        torch.cuda.synchronize(dev)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.time()
+        s.record(stream)
+        for _ in range(n):
+            fn()
+        e.record(stream)
+        torch.cuda.synchronize(dev)
+        clocks.mark(t0, time.time())
+        D.barrier()
+        return s.elapsed_time(e) / n
+
+    # -------------------------------------------------------------- headline prefill
+    w = synth.WORKLOADS[HEADLINE]
+    inp = synth.make_inputs(w.B, w.T, w.H, w.P, w.N, w.R, D.rank_seed(w.seed, rank), w.dtype)
+    d = to_dev(inp, dev, torch)
+    y = torch.empty(w.B, w.T, w.H, w.R, w.P, dtype=torch.float32, device=dev)
+    hT = m3.State.zeros(w.B, w.H, w.N, w.P, w.R, device=dev)
+    ws = m3.workspace_for(m3.M3Dims(), dev)
+
+    def prefill_step():
+        m3.m3_ssm_prefill(d["x"], d["B"], d["C"], d["dt"], d["A"], d["lambda"], d["theta"], y=y,
+                          hT=hT, workspace=ws)
+
+    for _ in range(args.warmup):
+        prefill_step()
+    ms = timed(prefill_step, args.steps)
+    if m3.m3_ssm_device_status(ws) != m3.M3_OK:
+        raise RuntimeError("device status reports a timed-out wait in the prefill kernel")
+    ms_max = D.max_over_ranks(ms, dev)
+    tokens = w.B * w.T
+    value = D.aggregate_throughput(tokens, world, ms_max / 1e3)
+    pb = prefill_bytes(w)
+    achieved = pb / (ms / 1e3) / 1e9
+    sha = kernel_source_sha()
+    kname = "prefill_tc_kernel<128,1>"
+    pf = prefill_flops(w)
+    in_bytes = sum(v.numel() * v.element_size() for v in d.values())
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "P": w.P, "N": w.N, "R": w.R,
+                   "chunk_tokens": CHUNK_ROWS // w.R, "in_dtype": "bf16", "out_dtype": "f32",
+                   "parallelism": f"replicas x{world}",
+                   "l2": (f"inputs larger than L2 ({in_bytes / 1e9:.2f} GB per step vs "
+                          f"{L2_BYTES / 1e6:.0f} MB)")},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": measured_traffic(kname, sha),
+                     "kernel": kname, "algorithmic_bytes_per_launch": pb,
+                     "peak_source": peaks["source"],
+                     "tensor_view": {"algorithmic_tflops": pf / (ms / 1e3) / 1e12,
+                                     "peak": peaks["bf16_tflops"],
+                                     "frac": pf / (ms / 1e3) / 1e12 / peaks["bf16_tflops"]}},
+        "gpu_launches": args.steps,
+    }
+
+    if not args.skip_extras:
+        # ---------------------------------------------------------- end to end (host buffers)
+        hin = {k: v.cpu().pin_memory() for k, v in d.items()}
+        hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        hh = torch.empty(hT.h.shape, dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            dd = {k: v.to(dev, non_blocking=True) for k, v in hin.items()}
+            m3.m3_ssm_prefill(dd["x"], dd["B"], dd["C"], dd["dt"], dd["A"], dd["lambda"],
+                              dd["theta"], y=y, hT=hT, workspace=ws)
+            hy.copy_(y, non_blocking=True)
+            hh.copy_(hT.h, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        ne = max(3, min(20, args.steps))
+        ms_e2e = D.max_over_ranks(timed(e2e_step, ne), dev)
+        line["e2e"] = {"value": D.aggregate_throughput(tokens, world, ms_e2e / 1e3),
+                       "unit": "tokens/s", "h2d_bytes_per_step": in_bytes,
+                       "d2h_bytes_per_step": y.numel() * 4 + hT.h.numel() * 4,
+                       "ms_per_step": ms_e2e}
+        line["gpu_launches"] += ne
+        del hin, hy, hh
+
+        # ---------------------------------------------------------- MIMO prefill
+        wm = synth.WORKLOADS[MIMO_PRE]
+        dm = to_dev(synth.make_inputs(wm.B, wm.T, wm.H, wm.P, wm.N, wm.R,
+                                      D.rank_seed(wm.seed, rank), wm.dtype), dev, torch)
+        ym = torch.empty(wm.B, wm.T, wm.H, wm.R, wm.P, dtype=torch.float32, device=dev)
+        hm = m3.State.zeros(wm.B, wm.H, wm.N, wm.P, wm.R, device=dev)
+
+        def fm():
+            m3.m3_ssm_prefill(dm["x"], dm["B"], dm["C"], dm["dt"], dm["A"], dm["lambda"],
+                              dm["theta"], y=ym, hT=hm, workspace=ws)
+
+        for _ in range(3):
+            fm()
+        msm = D.max_over_ranks(timed(fm, 20), dev)
+        bm = prefill_bytes(wm)
+        line["mimo_prefill"] = {
+            "workload": wm.name, "ms": msm,
+            "tokens_per_s": D.aggregate_throughput(wm.B * wm.T, world, msm / 1e3),
+            "achieved_gbs": bm / (msm / 1e3) / 1e9, "hbm_frac": bm / (msm / 1e3) / 1e9 / peaks["hbm_gbs"],
+            "algorithmic_tflops": prefill_flops(wm) / (msm / 1e3) / 1e12}
+        line["gpu_launches"] += 20
+        del dm, ym, hm
+
+        # ---------------------------------------------------------- decode loops
+        dec = {}
+        for name in (SISO_DEC, MIMO_DEC):
+            wd = synth.WORKLOADS[name]
+            seed = D.rank_seed(wd.seed, rank)
+            pre = to_dev(synth.make_inputs(wd.B, wd.prefill_T_for_decode, wd.H, wd.P, wd.N, wd.R,
+                                           seed, wd.dtype), dev, torch)
+            st = m3.State.zeros(wd.B, wd.H, wd.N, wd.P, wd.R, device=dev)
+
+            def reset_state():
+                m3.m3_ssm_prefill(pre["x"], pre["B"], pre["C"], pre["dt"], pre["A"], pre["lambda"],
+                                  pre["theta"], hT=st, workspace=ws)
+
+            nsteps = args.decode_steps
+            dsteps = []
+            for c0 in range(0, nsteps, 64):  # draw on the host in batches, keep on the device
+                seeds = [synth.decode_step_seed(seed, s) for s in range(c0, min(nsteps, c0 + 64))]
+                for si in gen_inputs_parallel(wd, seeds, A_seed=seed):
+                    t = to_dev(si, dev, torch)
+                    dsteps.append({k: (v[:, 0].contiguous() if k != "A" else v)
+                                   for k, v in t.items()})
+            yt = torch.empty(wd.B, wd.H, wd.R, wd.P, dtype=torch.float32, device=dev)
+
+            def step(q):
+                m3.m3_ssm_decode_step(st, q["x"], q["B"], q["C"], q["dt"], q["A"], q["lambda"],
+                                      q["theta"], y_t=yt)
+
+            def loop():
+                for q in dsteps:
+                    step(q)
+
+            reset_state()
+            for q in dsteps[:3]:  # warm-up steps, then back to the prefill state
+                step(q)
+            reset_state()
+            ms_loop = D.max_over_ranks(timed(loop, 1), dev)
+            per = ms_loop / nsteps
+            db = decode_bytes(wd)
+            dec[name] = {"steps": nsteps, "ms_total": ms_loop, "us_per_step": per * 1e3,
+                         "tokens_per_s": D.aggregate_throughput(wd.B, world, per / 1e3),
+                         "achieved_gbs": db / (per / 1e3) / 1e9,
+                         "hbm_frac": db / (per / 1e3) / 1e9 / peaks["hbm_gbs"],
+                         "algorithmic_bytes_per_step": db,
+                         "state_bytes": wd.B * wd.H * wd.N * wd.P * 4}
+            line["gpu_launches"] += nsteps
+            del dsteps, pre, st
+        line["decode"] = dec
+
+        # ---------------------------------------------------------- 16384-token prefill + decode
+        wl = synth.WORKLOADS[LONG]
+        lseed = D.rank_seed(wl.seed, rank)
+        dl = to_dev(synth.make_inputs(wl.B, wl.T, wl.H, wl.P, wl.N, wl.R, lseed, wl.dtype), dev,
+                    torch)
+        yl = torch.empty(wl.B, wl.T, wl.H, wl.R, wl.P, dtype=torch.float32, device=dev)
+        sl = m3.State.zeros(wl.B, wl.H, wl.N, wl.P, wl.R, device=dev)
+
+        def fl():
+            m3.m3_ssm_prefill(dl["x"], dl["B"], dl["C"], dl["dt"], dl["A"], dl["lambda"],
+                              dl["theta"], y=yl, hT=sl, workspace=ws)
+
+        for _ in range(3):
+            fl()
+        msl = D.max_over_ranks(timed(fl, 10), dev)
+        ldec = to_dev(synth.make_inputs(wl.B, wl.decode_steps, wl.H, wl.P, wl.N, wl.R, lseed + 100,
+                                        wl.dtype, A_seed=lseed), dev, torch)
+        lsteps = [{k: (v[:, s].contiguous() if k != "A" else v) for k, v in ldec.items()}
+                  for s in range(wl.decode_steps)]
+        ylt = torch.empty(wl.B, wl.H, wl.R, wl.P, dtype=torch.float32, device=dev)
+
+        def lloop():
+            for q in lsteps:
+                m3.m3_ssm_decode_step(sl, q["x"], q["B"], q["C"], q["dt"], q["A"], q["lambda"],
+                                      q["theta"], y_t=ylt)
+
+        msld = D.max_over_ranks(timed(lloop, 1), dev)
+        line["long"] = {"workload": wl.name, "prefill_ms": msl,
+                        "prefill_tokens_per_s": D.aggregate_throughput(wl.B * wl.T, world, msl / 1e3),
+                        "prefill_hbm_frac": prefill_bytes(wl) / (msl / 1e3) / 1e9 / peaks["hbm_gbs"],
+                        "decode_steps": wl.decode_steps,
+                        "decode_us_per_step": msld / wl.decode_steps * 1e3,
+                        "end_to_end_ms": msl + msld}
+        line["gpu_launches"] += 10 + wl.decode_steps
+
+    line["clocks"] = clocks.summary()
+
+    # -------------------------------------------------------------- CPU oracle baseline
+    if rank == 0 and world == 1 and not args.skip_extras:
+        v, used, done, spent = oracle_throughput(w, inp, budget_s=10.0)
+        line["cpu_baseline"] = {
+            "value": v, "unit": "tokens/s", "cores": used, "kind": "oracle",
+            "sample": (f"{done} of {w.B * w.H} (b,h) sequences x {w.T} tokens of the same "
+                       f"workload, {spent:.1f} s of fp64 oracle time; tokens counted as "
+                       f"sequences x T / H")}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    D.barrier()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
