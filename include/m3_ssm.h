@@ -133,6 +133,37 @@ m3_status m3_ssm_decode_step(const m3_dims* dims, const m3_state* state, const v
  */
 m3_status m3_ssm_device_status(void* workspace, void* stream);
 
+/*
+ * m3_ssm_prefill for callers that cannot allocate device memory.  The paper has
+ * no counterpart to this call; it exists for hosts that forbid device allocation
+ * once they are running (cudaMalloc synchronises the device and can fail under
+ * memory pressure), such as plugin hosts and serving loops, and for code whose
+ * whole memory budget belongs to a pool it does not control.
+ *
+ * Same arguments, layouts and results as m3_ssm_prefill, without the workspace:
+ * the scratch comes from a 4 MiB array in the library's device image, which
+ * every GPU that loads the library holds until the process exits.  The call
+ * allocates nothing (no cudaMalloc, no cudaFree, no allocating library routine).
+ *   - The first call on a device looks up the array's device address on the
+ *     current device (cudaGetSymbolAddress) and caches it; make that first call
+ *     before any stream capture on that device.
+ *   - Each call clears the part of the array it uses (cudaMemsetAsync on
+ *     `stream`) before the kernels run.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind: calls whose work overlaps on the GPU (different streams, no
+ *     ordering between them) race on it.  Order such calls on one stream.
+ *   - Returns M3_ERR_WORKSPACE if m3_ssm_prefill_workspace(dims) exceeds
+ *     4 MiB, M3_ERR_CUDA if the address lookup or the clear fails, and
+ *     otherwise whatever m3_ssm_prefill returns for the same arguments.
+ *   - A device-side wait that ran out is recorded in the array's status word,
+ *     which the caller cannot reach; it is cleared by the next call.  Callers
+ *     that need that report use m3_ssm_prefill with their own workspace.
+ */
+m3_status m3_ssm_prefill_noalloc(const m3_dims* dims, const void* x, const void* B, const void* C,
+                                 const void* dt, const float* A, const void* lambda,
+                                 const void* theta, const m3_state* h0, void* y,
+                                 const m3_state* hT, void* stream);
+
 /* Short English description of a status code (static storage). */
 const char* m3_status_str(m3_status s);
 

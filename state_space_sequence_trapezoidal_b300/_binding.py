@@ -60,6 +60,8 @@ def load() -> ctypes.CDLL:
             lib.m3_ssm_prefill_workspace.restype = sz
             lib.m3_ssm_prefill.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, sp, vp, sp, vp, sz, vp]
             lib.m3_ssm_prefill.restype = ctypes.c_int
+            lib.m3_ssm_prefill_noalloc.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, sp, vp, sp, vp]
+            lib.m3_ssm_prefill_noalloc.restype = ctypes.c_int
             lib.m3_ssm_decode_step.argtypes = [dp, sp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
             lib.m3_ssm_decode_step.restype = ctypes.c_int
             lib.m3_ssm_device_status.argtypes = [vp, vp]
@@ -175,6 +177,31 @@ def m3_ssm_prefill(x, B, C, dt, A, lam, theta, h0: State | None = None, *, y=Non
                                workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
     if st != M3_OK:
         raise M3Error(st, "m3_ssm_prefill")
+    return y
+
+
+def m3_ssm_prefill_noalloc(x, B, C, dt, A, lam, theta, h0: State | None = None, *, y,
+                           hT: State | None = None, out_dtype=torch.float32, stream=None):
+    """m3_ssm_prefill without a workspace, for callers that may not allocate device
+    memory: the library's own static device scratch is used instead.  ``y`` must be
+    given (this wrapper allocates nothing either).  Calls on one device share that
+    scratch, so calls that overlap on the GPU race; order them on one stream."""
+    in_dt = x.dtype
+    _check_inputs(dict(x=x, B=B, C=C, dt=dt, lam=lam, theta=theta), in_dt)
+    _check_inputs(dict(A=A), torch.float32)
+    d = _dims(x, dt, theta, 0, in_dt, out_dtype)
+    if y.dtype != out_dtype or not y.is_contiguous() or y.numel() != d.B * d.T * d.H * d.R * d.P:
+        raise ValueError("y: wrong dtype, layout or size")
+    c0 = h0._c() if h0 is not None else None
+    c1 = hT._c() if hT is not None else None
+    st = load().m3_ssm_prefill_noalloc(ctypes.byref(d), x.data_ptr(), B.data_ptr(), C.data_ptr(),
+                                       dt.data_ptr(), A.data_ptr(), lam.data_ptr(),
+                                       theta.data_ptr(),
+                                       ctypes.byref(c0) if c0 is not None else None, y.data_ptr(),
+                                       ctypes.byref(c1) if c1 is not None else None,
+                                       _stream_handle(stream))
+    if st != M3_OK:
+        raise M3Error(st, "m3_ssm_prefill_noalloc")
     return y
 
 
