@@ -55,7 +55,9 @@ typedef enum {
   M3_ERR_CUDA = 5,        /* a CUDA launch or call failed */
   M3_ERR_TIMEOUT = 6,     /* a device-side bounded wait ran out (see m3_ssm_device_status) */
   M3_ERR_UNSUPPORTED = 7, /* valid request this build does not implement (e.g. chunk value) */
-  M3_ERR_WORKSPACE = 8    /* workspace missing or smaller than m3_ssm_prefill_workspace() */
+  M3_ERR_WORKSPACE = 8,   /* workspace missing or smaller than m3_ssm_prefill_workspace() */
+  M3_ERR_RANGE = 9        /* an input exceeded the tensor-core path's fp16 operand range
+                             (see m3_ssm_prefill; reported by m3_ssm_device_status) */
 } m3_status;
 
 typedef enum { M3_F32 = 0, M3_BF16 = 1 } m3_dtype;
@@ -107,6 +109,14 @@ size_t m3_ssm_prefill_workspace(const m3_dims* dims);
  * bf16 inputs with P = 64, N in {64, 128}, R in {1, 2, 4, 8} run on the
  * tcgen05 tensor-core kernel; every other supported shape, and fp32 inputs,
  * run on a CUDA-core recurrent kernel with fp32 arithmetic.
+ *
+ * Tensor-core operands: the rotated B and C and the products dt-weight * x are
+ * held as fp16 (the state copy is rescaled per chunk, the masked scores are
+ * bf16 hi + lo pairs), with fp32 accumulation; the result is within about 1% of
+ * the output RMS of the exact recurrence.  An operand value beyond the fp16
+ * range (|B|, |C| above about 46000, or |x| times the step weight above 65504)
+ * makes m3_ssm_device_status report M3_ERR_RANGE for that call; its outputs
+ * are then invalid.
  */
 m3_status m3_ssm_prefill(const m3_dims* dims, const void* x, const void* B, const void* C,
                          const void* dt, const float* A, const void* lambda, const void* theta,
@@ -129,7 +139,9 @@ m3_status m3_ssm_decode_step(const m3_dims* dims, const m3_state* state, const v
 /*
  * Waits for `stream`, then reads and clears the device status word kept in
  * `workspace`.  Returns M3_OK, M3_ERR_TIMEOUT (a bounded wait inside a
- * prefill kernel ran out; that call's outputs are invalid), or M3_ERR_CUDA.
+ * prefill kernel ran out; that call's outputs are invalid), M3_ERR_RANGE (an
+ * operand exceeded the tensor-core path's fp16 range; outputs invalid), or
+ * M3_ERR_CUDA.
  */
 m3_status m3_ssm_device_status(void* workspace, void* stream);
 

@@ -18,6 +18,7 @@ from . import build as _build
 
 M3_OK = 0
 M3_ERR_TIMEOUT = 6
+M3_ERR_RANGE = 9
 M3_F32, M3_BF16 = 0, 1
 _DT = {torch.float32: M3_F32, torch.bfloat16: M3_BF16}
 

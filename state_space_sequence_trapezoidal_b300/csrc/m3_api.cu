@@ -57,6 +57,7 @@ const char* m3_status_str(m3_status s) {
     case M3_ERR_TIMEOUT: return "device-side wait timed out";
     case M3_ERR_UNSUPPORTED: return "request not supported by this build";
     case M3_ERR_WORKSPACE: return "workspace missing or too small";
+    case M3_ERR_RANGE: return "operand outside the tensor-core path's fp16 range";
   }
   return "unknown status";
 }
@@ -141,7 +142,8 @@ m3_status m3_ssm_device_status(void* workspace, void* stream) {
   if (word == 0) return M3_OK;
   if (cudaMemsetAsync(workspace, 0, sizeof(word), s) != cudaSuccess) return M3_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return M3_ERR_CUDA;
-  return (word & m3::kDevTimeout) ? M3_ERR_TIMEOUT : M3_ERR_CUDA;
+  if (word & m3::kDevTimeout) return M3_ERR_TIMEOUT;
+  return (word & m3::kDevRange) ? M3_ERR_RANGE : M3_ERR_CUDA;
 }
 
 }  // extern "C"

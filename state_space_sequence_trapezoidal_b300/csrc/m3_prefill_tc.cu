@@ -11,26 +11,37 @@
 // because beta_{j+1} = q_{j+1} alpha_{j+1} and alpha_{j+1} = exp(l_{j+1} - l_j).
 // With H the state carried into the chunk (the previous chunk's last-token
 // term already folded in), per chunk of 128 (token, rank) rows:
-//     S = C~ B~^T                                  (GEMM1, 128 x 128 x N)
-//     Y = (M (x) J_R o S) X + diag(e^{l}) C~ H     (GEMM2, GEMM3)
+//     S = C~ B~^T                                   (GEMM1, 128 x 128 x N)
+//     Y = (M (x) J_R o S) X + diag(e^{l}) C~ H      (GEMM2, GEMM3)
 //     H <- e^{l_last} H + B~^T diag(d) X,  d_j = e^{l_last - l_j} w_j   (GEMM4)
 // where w of the chunk's last token takes q of the next chunk's first token,
 // which carries the trapezoid's previous-token term across the boundary.
+// B~, C~ are B, C rotated by the cumulative angle (Proposition 3).
 //
-// Kernel design (one CTA per (batch row, head), two CTAs per SM, 256 threads):
-//  * B, C, X tiles of 128 rows arrive by TMA (128-byte swizzle, zero fill past T).
-//  * All threads rotate B and C in place in shared memory by the cumulative angle
-//    (a prefix sum over the chunk plus the carried angle), Proposition 3.
-//  * One thread issues the four GEMMs (tcgen05.mma kind::f16, bf16 operands,
-//    fp32 accumulators in TMEM).  The mask is applied between GEMM1 and GEMM2 by
-//    all eight warps reading S from TMEM.  The fp32 state H stays in TMEM across
-//    the whole sequence; a bf16 copy in shared memory feeds GEMM3.
-//  * Decay factors are kept as log2 sums and only non-positive differences are
-//    exponentiated, so nothing overflows however long the chunk.
-// TMEM (256 columns): [0,128) S, later U = B~^T diag(d) X in [0,64);
-//                     [128,192) Y; [192,256) H (fp32, N lanes x 64 columns).
+// Kernel design: one CTA per (batch row, head) sequence, 10 warps with fixed roles,
+// chunks flow through a two-stage pipeline so that loads, CUDA-core work and
+// tensor-core work of neighbouring chunks overlap:
+//   warp 0      TMA producer: raw bf16 tiles of B, C and X (128-byte swizzle) into
+//               one of two stages.
+//   warp 1      MMA issuer (one thread): GEMM1, GEMM4, GEMM3, GEMM2 per chunk.
+//   warps 2-5   transform: discretisation (decay log-sums, trapezoid weights), the
+//               cumulative angle, rotation of B and C in place to fp16, and the
+//               d-scaled copy of X in fp16.  theta, dt and lambda are prefetched
+//               into registers one chunk ahead.
+//   warps 6-9   epilogue (one thread per TMEM lane): mask the scores in TMEM into
+//               bf16 hi/lo pairs (GEMM2 reads them from TMEM), advance the fp32
+//               state (kept in registers) and write its scaled fp16 copy for
+//               GEMM3, and write y.
+// Operand precision: B~, C~, the state copy and d X are fp16 (11 significant
+// bits; the state copy carries a per-chunk power-of-two scale), the masked scores
+// are bf16 hi + lo (about 16 bits, full fp32 range), X is the exact bf16 input;
+// every product accumulates in fp32 in TMEM.  The measured error of this scheme
+// is about 0.6-0.8% of the output RMS at the benchmark shapes.
+// TMEM (512 columns): [0,256) two score buffers, [256,320) C~H, [320,384) PX,
+// [384,448) the chunk's state increment U.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <stdint.h>
@@ -41,13 +52,33 @@
 namespace m3 {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kRows = 128;         // (token, rank) rows per chunk
-constexpr int kP = 64;             // head dimension handled by this kernel
-constexpr uint32_t kTmemCols = 256;
+constexpr int kRows = 128;  // (token, rank) rows per chunk
+constexpr int kP = 64;      // head dimension handled by this kernel
+constexpr int kThreads = 320;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpXf = 2, kWarpEpi = 6;
+constexpr int kRole = 128;  // threads of the transform and of the epilogue role
+constexpr uint32_t kBarXf = 1, kBarEpi = 2;  // named barrier ids
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t TM_S = 0, TM_YOFF = 256, TM_YIN = 320, TM_U = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kTwoPi = 6.283185307179586f;
 constexpr float kInvTwoPi = 0.15915494309189535f;
+constexpr float kF16Max = 65504.f;
+
+// mbarriers
+enum {
+  B_FULL = 0,    // [2] TMA tiles of a stage landed
+  B_SFREE = 2,   // [2] stage and score buffer free again (commit after GEMM2)
+  B_XF = 4,      // [2] transform finished a chunk (4 warp arrivals)
+  B_SFULL = 6,   // [2] scores in TMEM (commit after GEMM1)
+  B_PFULL = 8,   // [2] masked scores written back (4 warp arrivals)
+  B_UFULL = 10,  // state increment U in TMEM (commit after GEMM4)
+  B_STATE = 11,  // state advanced: U read, next h^T copy in shared memory (4 arrivals)
+  B_HFREE = 12,  // GEMM3 finished reading h^T (commit)
+  B_YFULL = 13,  // GEMM2 finished: both output accumulators complete (commit)
+  B_YFREE = 14,  // epilogue read both output accumulators (4 arrivals)
+  NUM_BARS = 15
+};
 
 struct TcParams {
   CUtensorMap tmB;  // B [B][T][H][R][N] bf16, box {64, R, 1, CT, 1}
@@ -75,45 +106,41 @@ struct TcParams {
 
 template <int NS, int R>
 struct Cfg {
-  static constexpr int CT = kRows / R;               // tokens per chunk
-  static constexpr int NB = NS / 64;                 // 64-wide blocks of the state dim
-  static constexpr int K = NS / 2;                   // rotation pairs
-  static constexpr int PG = K / 4;                   // 16-byte groups (4 pairs) per row
-  static constexpr int TB = (kThreads / PG < CT) ? kThreads / PG : CT;  // token blocks
-  static constexpr int TPT = CT / TB;                // tokens per rotation thread
+  static constexpr int CT = kRows / R;   // tokens per chunk
+  static constexpr int NB = NS / 64;     // 64-wide blocks of the state dimension
+  static constexpr int K = NS / 2;       // rotation pairs
+  static constexpr int PG = K / 4;       // 16-byte groups (4 pairs) per row
+  static constexpr int TB = kRole / PG;  // token blocks of the rotation
+  static constexpr int TPT = CT / TB;    // tokens per rotation thread
   static constexpr int kLogR = R == 1 ? 0 : R == 2 ? 1 : R == 4 ? 2 : 3;
-  // Shared memory map (bytes from a 1024-aligned base).  Every rounded GEMM operand is
-  // held as a bf16 pair (hi, lo) with hi = bf16(v), lo = bf16(v - hi).
-  static constexpr uint32_t TILE = NB * 16384;        // one 128-row tile of width NS
-  static constexpr uint32_t OFF_B = 0;                // B~ hi   [NB][128 rows][128 B]
-  static constexpr uint32_t OFF_C = OFF_B + TILE;     // C~ hi
-  static constexpr uint32_t OFF_BL = OFF_C + TILE;    // B~ lo
-  static constexpr uint32_t OFF_CL = OFF_BL + TILE;   // C~ lo
-  static constexpr uint32_t OFF_X = OFF_CL + TILE;    // X (exact bf16)
-  static constexpr uint32_t OFF_H = OFF_X + 16384;    // state hi  [NB][64 p][128 B]
-  static constexpr uint32_t OFF_HL = OFF_H + NB * 8192;  // state lo
-  static constexpr uint32_t OFF_P = OFF_B;            // masked scores hi (32 KB: B, and C if NB == 1)
-  static constexpr uint32_t OFF_PL = OFF_BL;          // masked scores lo
-  static constexpr uint32_t OFF_MISC = OFF_HL + NB * 8192;
-  // misc (floats)
-  static constexpr int M_DT = 0;
-  static constexpr int M_ELL = M_DT + CT;
-  static constexpr int M_GAM = M_ELL + CT;
-  static constexpr int M_WGT = M_GAM + CT;
-  static constexpr int M_DSC = M_WGT + CT;
-  static constexpr int M_EL = M_DSC + CT;
-  static constexpr int M_Q = M_EL + CT;               // CT + 1 entries
-  static constexpr int M_SCAL = M_Q + CT + 4;         // [0] e^{l_last}
-  static constexpr int M_CARRY = M_SCAL + 4;          // [2][64]
-  static constexpr int M_SCAN = M_CARRY + 2 * 64;     // [TB][K], also [R][NS] + [R][64] at entry
-  static constexpr int SCAN_FLOATS = (TB * K > R * NS + R * 64) ? TB * K : R * NS + R * 64;
-  static constexpr int M_END = M_SCAN + SCAN_FLOATS;
+  // shared memory (bytes from a 1024-aligned base)
+  static constexpr uint32_t TILE = NB * 16384;        // 128 rows x NS, bf16 or fp16
+  static constexpr uint32_t STAGE = 2 * TILE + 16384;  // B~, C~, X
+  static constexpr uint32_t OFF_DX = 2 * STAGE;        // d X, fp16 [128 rows][64]
+  static constexpr uint32_t OFF_H = OFF_DX + 16384;    // h^T, fp16 [NB][64 p][64 n]
+  static constexpr uint32_t OFF_MISC = OFF_H + NB * 8192;
+  // misc floats
+  static constexpr int M_ELL = 0;             // [2][128] decay log2-sums
+  static constexpr int M_W = 256;             // [2][128] trapezoid column weights
+  static constexpr int M_GAM = 512;           // [2][128] diagonal weights
+  static constexpr int M_EL = 768;            // [2][128] 2^{l}
+  static constexpr int M_ELAST = 1024;        // [2] 2^{l_last}
+  static constexpr int M_D = 1028;            // [128] d_j
+  static constexpr int M_DT = 1156;           // [128] dt
+  static constexpr int M_Q = 1284;            // [129] q, then q of the next chunk's first token
+  static constexpr int M_WSUM = 1416;         // [4] warp totals of the log2-decay scan
+  static constexpr int M_HMAX = 1420;         // [2][4] per-warp max |h|
+  static constexpr int M_CARRY = 1428;        // [2][64] angle carried into a chunk
+  static constexpr int M_SCAN = 1556;         // [TB][K] angle partial sums
+  static constexpr int M_END = M_SCAN + TB * K;
   static constexpr uint32_t OFF_BAR = OFF_MISC + ((M_END * 4 + 15) / 16) * 16;
-  static constexpr uint32_t SMEM_USED = OFF_BAR + 32;
+  static constexpr uint32_t OFF_HOLD = OFF_BAR + NUM_BARS * 8;  // TMEM base, abort flag
+  static constexpr uint32_t SMEM_USED = OFF_HOLD + 16;
   static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
   static_assert(kRows % R == 0, "R must divide 128");
   static_assert(NS == 64 || NS == 128, "N must be 64 or 128");
   static_assert(TB * TPT == CT, "token split");
+  static_assert(CT <= kRole, "one discretisation thread per token");
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory");
 };
 
@@ -134,11 +161,14 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-__device__ __forceinline__ void store_split_bf16(uint8_t* hi_base, uint8_t* lo_base, uint32_t off,
-                                                 float v) {
-  const __nv_bfloat16 h = __float2bfloat16_rn(v);
-  *reinterpret_cast<__nv_bfloat16*>(hi_base + off) = h;
-  *reinterpret_cast<__nv_bfloat16*>(lo_base + off) = __float2bfloat16_rn(v - __bfloat162float(h));
+// Power of two s with max_abs * s in [2^14, 2^15): the fp16 state copy keeps full
+// relative precision and stays far from overflow.  1 for a zero (or denormal) state.
+__device__ __forceinline__ float state_scale(float max_abs) {
+  const int e = (__float_as_int(max_abs) >> 23) & 0xff;
+  if (e == 0) return 1.f;
+  int f = 268 - e;  // exponent field of 2^(141 - e)
+  f = f < 1 ? 1 : (f > 254 ? 254 : f);
+  return __int_as_float(f << 23);
 }
 
 template <int NS, int R>
@@ -150,23 +180,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(sm);
-  const uint32_t sB = sbase + C::OFF_B, sC = sbase + C::OFF_C, sBl = sbase + C::OFF_BL,
-                 sCl = sbase + C::OFF_CL, sX = sbase + C::OFF_X, sH = sbase + C::OFF_H,
-                 sHl = sbase + C::OFF_HL, sP = sbase + C::OFF_P, sPl = sbase + C::OFF_PL;
   float* misc = reinterpret_cast<float*>(sm + C::OFF_MISC);
-  float* s_dt = misc + C::M_DT;
-  float* s_ell = misc + C::M_ELL;
-  float* s_gam = misc + C::M_GAM;
-  float* s_wgt = misc + C::M_WGT;
-  float* s_dsc = misc + C::M_DSC;
-  float* s_eL = misc + C::M_EL;
-  float* s_q = misc + C::M_Q;
-  float* s_scal = misc + C::M_SCAL;
-  float* s_carry = misc + C::M_CARRY;
-  float* s_scan = misc + C::M_SCAN;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + C::OFF_BAR + 16);
-  const uint32_t bar_tma = smem_u32(&bars[0]), bar_mma = smem_u32(&bars[1]);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + C::OFF_HOLD);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(sm + C::OFF_HOLD + 4);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x, b = bh / p.H, head = bh % p.H, H = p.H;
@@ -175,15 +193,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   const float A2 = p.A[head] * kLog2e;
 
   if (tid == 0) {
-    mbar_init(bar_tma, 1);
-    mbar_init(bar_mma, 1);
+    const int counts[NUM_BARS] = {1, 1, 1, 1, 4, 4, 1, 1, 4, 4, 1, 4, 1, 1, 4};
+    for (int i = 0; i < NUM_BARS; ++i) mbar_init(bar(i), counts[i]);
+    *s_abort = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
     tma_prefetch_desc(&p.tmB);
     tma_prefetch_desc(&p.tmC);
     tma_prefetch_desc(&p.tmX);
   }
-  if (warp == 0) {
+  if (warp == kWarpMma) {
     tmem_alloc(smem_u32(s_tmem), kTmemCols);
     tmem_relinquish();
   }
@@ -191,455 +210,524 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  const uint32_t tS = tmem, tU = tmem, tY = tmem + 128, tHc = tmem + 192;
-  const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-  const int trow = (warp & 3) * 32 + lane;  // TMEM lane / tile row owned by this thread
-  const int half = warp >> 2;               // which half of the columns
 
-  auto issue_tma = [&](int ck) {
-    mbar_arrive_expect_tx(bar_tma, (2 * NB + 1) * 16384);
+  if (warp == kWarpTma) {
+    // ================================================================ TMA producer
+    if (lane == 0) {
+      int issued[2] = {-1, -1};
+      for (int k = 0; k < nchunks; ++k) {
+        const int s = k & 1;
+        if (k >= 2 && !mbar_wait_abortable(bar(B_SFREE + s), ((k >> 1) - 1) & 1, s_abort)) break;
+        const uint32_t st = sbase + s * C::STAGE;
+        mbar_arrive_expect_tx(bar(B_FULL + s), C::STAGE);
 #pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-      tma_load_5d(sB + nb * 16384, &p.tmB, bar_tma, 64 * nb, 0, head, ck * CT, b);
-      tma_load_5d(sC + nb * 16384, &p.tmC, bar_tma, 64 * nb, 0, head, ck * CT, b);
-    }
-    tma_load_5d(sX, &p.tmX, bar_tma, 0, 0, head, ck * CT, b);
-  };
-  if (tid == 0 && nchunks > 0) issue_tma(0);
-
-  // Writes H (fp32) of state row n, columns 32*half .. +31, into TMEM and its hi/lo copy
-  // into the K-major B operand of GEMM3 (row p, column n of [NB][64][128 B]).
-  auto put_state = [&](uint32_t (&hv)[32]) {
-    const int n = trow;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int pc = 32 * half + j;
-      const uint32_t off = (n >> 6) * 8192u + sw128(pc, (n & 63) >> 3) + (n & 7) * 2;
-      store_split_bf16(sm + C::OFF_H, sm + C::OFF_HL, off, __uint_as_float(hv[j]));
-    }
-    tmem_st32(tHc + lane_off + 32 * half, hv);
-    tmem_st_wait();
-  };
-
-  // ---------------------------------------------------------------- entry state
-  // H' = h0 + q_0 B~_{-1} X_{-1}^T, with B~_{-1} the stored previous token rotated by
-  // its own angle phi0 and q_0 = (1 - lambda_0) dt_0 of this call's first token.
-  {
-    float* s_fb = s_scan;            // [R][NS]
-    float* s_fx = s_scan + R * NS;   // [R][64]
-    for (int k = tid; k < K; k += kThreads) {
-      const float ph = p.phi0 ? p.phi0[static_cast<size_t>(bh) * K + k] : 0.f;
-      s_carry[k] = reduce_angle(ph);
-      float s, c;
-      sincosf(ph, &s, &c);
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        float u = 0.f, v = 0.f;
-        if (p.prevB0) {
-          const __nv_bfloat16* pb = p.prevB0 + (static_cast<size_t>(bh) * R + r) * NS + 2 * k;
-          u = __bfloat162float(pb[0]);
-          v = __bfloat162float(pb[1]);
+        for (int nb = 0; nb < NB; ++nb) {
+          tma_load_5d(st + nb * 16384, &p.tmB, bar(B_FULL + s), 64 * nb, 0, head, k * CT, b);
+          tma_load_5d(st + C::TILE + nb * 16384, &p.tmC, bar(B_FULL + s), 64 * nb, 0, head, k * CT, b);
         }
-        s_fb[r * NS + 2 * k] = c * u + s * v;
-        s_fb[r * NS + 2 * k + 1] = -s * u + c * v;
+        tma_load_5d(st + 2 * C::TILE, &p.tmX, bar(B_FULL + s), 0, 0, head, k * CT, b);
+        issued[s] = k;
       }
+      // no copy may still be in flight when the CTA exits
+      for (int s = 0; s < 2; ++s)
+        if (issued[s] >= 0) mbar_wait(bar(B_FULL + s), (issued[s] >> 1) & 1);
     }
-    for (int i = tid; i < R * kP; i += kThreads)
-      s_fx[i] = p.prevx0 ? __bfloat162float(p.prevx0[static_cast<size_t>(bh) * R * kP + i]) : 0.f;
-    __syncthreads();
-    float q0 = 0.f;
-    if (T > 0) {
-      const size_t o = static_cast<size_t>(b) * T * H + head;  // token 0
-      const float d0 = __bfloat162float(p.dt[o]), l0 = __bfloat162float(p.lam[o]);
-      q0 = (1.f - l0) * d0;
-    }
-    if ((warp & 3) * 32 < NS) {  // warp-uniform: this warp owns state rows
-      const int n = trow;
-      uint32_t hv[32];
+  } else if (warp == kWarpMma) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t I_S = idesc_f16(128, 128, 0, 0);   // S = C~ B~^T
+      constexpr uint32_t I_CH = idesc_f16(128, 64, 0, 0);   // Y_off = C~ H
+      constexpr uint32_t I_U = idesc_f16(128, 64, 1, 1);    // U = B~^T (d X)
+      constexpr uint32_t I_PX = idesc_bf16(128, 64, 0, 1);  // Y_in = P X
+      const uint32_t sDX = sbase + C::OFF_DX, sH = sbase + C::OFF_H;
+      int last_bar = -1;
+      uint32_t last_par = 0;
+      for (int k = 0; k < nchunks; ++k) {
+        const int s = k & 1;
+        const uint32_t st = sbase + s * C::STAGE;
+        const uint32_t sB = st, sC = st + C::TILE, sX = st + 2 * C::TILE;
+        const uint32_t tS = tmem + TM_S + 128u * s;
+        if (!mbar_wait_abortable(bar(B_XF + s), (k >> 1) & 1, s_abort)) break;
+        if (k >= 2 && !mbar_wait_abortable(bar(B_SFREE + s), ((k >> 1) - 1) & 1, s_abort)) break;
+        tc_fence_after();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int pc = 32 * half + j;
-        float v = p.h0 ? p.h0[(static_cast<size_t>(bh) * NS + n) * kP + pc] : 0.f;
-        float f = 0.f;
-#pragma unroll
-        for (int r = 0; r < R; ++r) f = fmaf(s_fb[r * NS + n], s_fx[r * kP + pc], f);
-        hv[j] = __float_as_uint(fmaf(q0, f, v));
-      }
-      put_state(hv);
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-  }
-
-  // Instruction descriptors (M = 128 rows throughout).
-  constexpr uint32_t I_S = idesc_bf16(128, 128, 0, 0);  // S = C~ B~^T
-  constexpr uint32_t I_CH = idesc_bf16(128, 64, 0, 0);  // Y = C~ H
-  constexpr uint32_t I_U = idesc_bf16(128, 64, 1, 1);   // U = B~^T X  (both MN-major)
-  constexpr uint32_t I_PX = idesc_bf16(128, 64, 0, 1);  // Y += P X   (X MN-major)
-
-  uint32_t mma_count = 0;
-  bool ok = true;
-
-  const bool rot_thread = tid < PG * TB;
-  const int pg = tid % PG, tb = tid / PG;
-
-  for (int ck = 0; ck < nchunks; ++ck) {
-    const int t0 = ck * CT;
-    // ------------------------------------------------------------ discretisation
-    if (warp == 0) {
-      constexpr int TPL = (CT + 31) / 32;
-      float a2[TPL], gm[TPL], qq[TPL];
-      float run = 0.f;
-#pragma unroll
-      for (int u = 0; u < TPL; ++u) {
-        const int i = lane * TPL + u;
-        const int t = t0 + i;
-        float d = 0.f, l = 0.f;
-        if (i < CT && t < T) {
-          const size_t o = (static_cast<size_t>(b) * T + t) * H + head;
-          d = __bfloat162float(p.dt[o]);
-          l = __bfloat162float(p.lam[o]);
+        for (int ks = 0; ks < KS; ++ks) {
+          const uint32_t ko = (ks >> 2) * 16384u + (ks & 3) * 32u;
+          tc_mma_ss(tS, sdesc_sw128(sC + ko, 16, 1024), sdesc_sw128(sB + ko, 16, 1024), I_S, ks > 0);
         }
-        run += d * A2;
-        a2[u] = run;
-        gm[u] = l * d;
-        qq[u] = (1.f - l) * d;
-        if (i < CT) s_dt[i] = d;
+        tc_commit(bar(B_SFULL + s));
+        last_bar = B_SFULL + s;
+        last_par = (k >> 1) & 1;
+        if (!mbar_wait_abortable(bar(B_STATE), k & 1, s_abort)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < kRows / 16; ++ks) {
+          const uint32_t kr = ks * 2048u;
+          tc_mma_ss(tmem + TM_U, sdesc_sw128(sB + kr, 16384, 1024), sdesc_sw128(sDX + kr, 16384, 1024),
+                    I_U, ks > 0);
+        }
+        tc_commit(bar(B_UFULL));
+        last_bar = B_UFULL;
+        last_par = k & 1;
+        if (k >= 1 && !mbar_wait_abortable(bar(B_YFREE), (k - 1) & 1, s_abort)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const uint32_t ka = (ks >> 2) * 16384u + (ks & 3) * 32u;
+          const uint32_t kh = (ks >> 2) * 8192u + (ks & 3) * 32u;
+          tc_mma_ss(tmem + TM_YOFF, sdesc_sw128(sC + ka, 16, 1024), sdesc_sw128(sH + kh, 16, 1024), I_CH,
+                    ks > 0);
+        }
+        tc_commit(bar(B_HFREE));
+        last_bar = B_HFREE;
+        last_par = k & 1;
+        if (!mbar_wait_abortable(bar(B_PFULL + s), (k >> 1) & 1, s_abort)) break;
+        tc_fence_after();
+        // masked scores as A from TMEM: per 32-column block, 16 columns of bf16 hi pairs
+        // then 16 columns of lo pairs; each MMA takes K = 16 rows of X.
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk)
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int sub = 0; sub < 2; ++sub) {
+              const uint32_t j0 = 32u * blk + 16u * sub;
+              tc_mma_ts(tmem + TM_YIN, tS + 32u * blk + 16u * part + 8u * sub,
+                        sdesc_sw128(sX + j0 * 128u, 16384, 1024), I_PX, (blk | part | sub) != 0);
+            }
+        tc_commit(bar(B_YFULL));
+        tc_commit(bar(B_SFREE + s));
+        last_bar = B_SFREE + s;
+        last_par = (k >> 1) & 1;
       }
-      float incl = run;
+      // every MMA must be complete before the TMEM is released (the last commit tracks all)
+      if (last_bar >= 0) mbar_wait(bar(last_bar), last_par);
+    }
+  } else if (warp < kWarpEpi) {
+    // ================================================================ transform
+    const int xt = tid - kWarpXf * 32;  // 0..127
+    const int xw = xt >> 5;
+    const int pg = xt % PG, tb = xt / PG;
+    float* s_ell = misc + C::M_ELL;
+    float* s_w = misc + C::M_W;
+    float* s_gam = misc + C::M_GAM;
+    float* s_el = misc + C::M_EL;
+    float* s_elast = misc + C::M_ELAST;
+    float* s_d = misc + C::M_D;
+    float* s_dt = misc + C::M_DT;
+    float* s_q = misc + C::M_Q;
+    float* s_wsum = misc + C::M_WSUM;
+    float* s_carry = misc + C::M_CARRY;
+    float* s_scan = misc + C::M_SCAN;
+    const size_t tok_stride = static_cast<size_t>(H);
+    const size_t seq0 = static_cast<size_t>(b) * T * H + head;  // token 0 of this sequence
+
+    auto load_tok = [&](int kk, float& d, float& l) {
+      const int t = kk * CT + xt;
+      d = 0.f;
+      l = 0.f;
+      if (xt < CT && t < T) {
+        d = __bfloat162float(p.dt[seq0 + t * tok_stride]);
+        l = __bfloat162float(p.lam[seq0 + t * tok_stride]);
+      }
+    };
+    auto load_q = [&](int kk) -> float {
+      const int t = kk * CT;
+      if (xt != 0 || t >= T) return 0.f;
+      return (1.f - __bfloat162float(p.lam[seq0 + t * tok_stride])) *
+             __bfloat162float(p.dt[seq0 + t * tok_stride]);
+    };
+    auto load_th = [&](int kk, uint2 (&th)[TPT]) {
+#pragma unroll
+      for (int u = 0; u < TPT; ++u) {
+        const int t = kk * CT + tb * TPT + u;
+        th[u] = make_uint2(0u, 0u);
+        if (t < T)
+          th[u] = *reinterpret_cast<const uint2*>(p.theta + (seq0 + t * tok_stride) * K + 4 * pg);
+      }
+    };
+
+    float cur_dt, cur_lam, nxt_dt = 0.f, nxt_lam = 0.f;
+    uint2 th_cur[TPT], th_nxt[TPT];
+    load_tok(0, cur_dt, cur_lam);
+    float qn_cur = load_q(1), qn_nxt = 0.f;
+    load_th(0, th_cur);
+#pragma unroll
+    for (int u = 0; u < TPT; ++u) th_nxt[u] = make_uint2(0u, 0u);
+    for (int k = xt; k < K; k += kRole) s_carry[k] = reduce_angle(p.phi0 ? p.phi0[static_cast<size_t>(bh) * K + k] : 0.f);
+    float range = 0.f;  // largest |value| converted to fp16
+    bool ab = false;
+
+    for (int k = 0; k < nchunks; ++k) {
+      const int s = k & 1;
+      if (k + 1 < nchunks) {
+        load_tok(k + 1, nxt_dt, nxt_lam);
+        load_th(k + 1, th_nxt);
+      }
+      qn_nxt = load_q(k + 2);
+      // ---------------------------------------------------------- step A: decay scan
+      const float a2 = cur_dt * A2;
+      const float gam = cur_lam * cur_dt;
+      float incl = a2;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const float v = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += v;
       }
-      const float excl = incl - run;
+      if (lane == 31) s_wsum[xw] = incl;
+      if (xt < CT) {
+        s_q[xt] = (1.f - cur_lam) * cur_dt;
+        s_dt[xt] = cur_dt;
+      }
+      if (xt == 0) s_q[CT] = qn_cur;
+      // the epilogue must be done with this misc slot (chunk k - 2)
+      if (k >= 2) ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_PFULL + s), ((k >> 1) - 1) & 1, s_abort));
+      if (bar_sync_or(kBarXf, kRole, ab)) { ab = true; break; }
+      // ---------------------------------------------------------- step B: weights, angle partials
+      {
+        float ell = incl, ltot = 0.f;
 #pragma unroll
-      for (int u = 0; u < TPL; ++u) {
-        const int i = lane * TPL + u;
-        if (i < CT) {
-          s_ell[i] = excl + a2[u];
-          s_gam[i] = gm[u];
-          s_q[i] = qq[u];
+        for (int w = 0; w < 4; ++w) {
+          const float v = s_wsum[w];
+          ltot += v;
+          if (w < xw) ell += v;
         }
-      }
-      if (lane == 0) {
-        const int t = t0 + CT;
-        float qn = 0.f;
-        if (t < T) {
-          const size_t o = (static_cast<size_t>(b) * T + t) * H + head;
-          qn = (1.f - __bfloat162float(p.lam[o])) * __bfloat162float(p.dt[o]);
+        if (xt < CT) {
+          const float w = gam + s_q[xt + 1];
+          s_ell[s * 128 + xt] = ell;
+          s_w[s * 128 + xt] = w;
+          s_gam[s * 128 + xt] = gam;
+          s_el[s * 128 + xt] = ex2(ell);
+          s_d[xt] = ex2(ltot - ell) * w;
         }
-        s_q[CT] = qn;
-      }
-      __syncwarp();
-      const float ell_last = s_ell[CT - 1];
+        if (xt == 0) s_elast[s] = ex2(ltot);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int u = 0; u < TPL; ++u) {
-        const int i = lane * TPL + u;
-        if (i < CT) {
-          const float w = s_gam[i] + s_q[i + 1];
-          s_wgt[i] = w;
-          s_dsc[i] = ex2(ell_last - s_ell[i]) * w;
-          s_eL[i] = ex2(s_ell[i]);
+        for (int u = 0; u < TPT; ++u) {
+          const float d = s_dt[tb * TPT + u];
+          const float2 t01 = unpack_bf16x2(th_cur[u].x), t23 = unpack_bf16x2(th_cur[u].y);
+          acc[0] = fmaf(d, t01.x, acc[0]);
+          acc[1] = fmaf(d, t01.y, acc[1]);
+          acc[2] = fmaf(d, t23.x, acc[2]);
+          acc[3] = fmaf(d, t23.y, acc[3]);
+        }
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) s_scan[tb * K + 4 * pg + qq] = acc[qq];
+      }
+      if (bar_sync_or(kBarXf, kRole, ab)) { ab = true; break; }
+      // ---------------------------------------------------------- step C: rotate B, C; d X
+      {
+        float ang[4];
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) ang[qq] = s_carry[s * 64 + 4 * pg + qq];
+        for (int t2 = 0; t2 < tb; ++t2)
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) ang[qq] += s_scan[t2 * K + 4 * pg + qq];
+        ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_FULL + s), (k >> 1) & 1, s_abort));
+        if (!ab) {
+          uint8_t* stg = sm + s * C::STAGE;
+          const int nb = pg >> 3, c16 = pg & 7;
+#pragma unroll
+          for (int u = 0; u < TPT; ++u) {
+            const float d = s_dt[tb * TPT + u];
+            const float2 t01 = unpack_bf16x2(th_cur[u].x), t23 = unpack_bf16x2(th_cur[u].y);
+            ang[0] = fmaf(d, t01.x, ang[0]);
+            ang[1] = fmaf(d, t01.y, ang[1]);
+            ang[2] = fmaf(d, t23.x, ang[2]);
+            ang[3] = fmaf(d, t23.y, ang[3]);
+            float cs[4], sn[4];
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) __sincosf(reduce_angle(ang[qq]), &sn[qq], &cs[qq]);
+            const int i = tb * TPT + u;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              const uint32_t off = nb * 16384u + sw128(i * R + r, c16);
+              uint4 vb = *reinterpret_cast<const uint4*>(stg + off);
+              uint4 vc = *reinterpret_cast<const uint4*>(stg + C::TILE + off);
+              uint32_t* wb = reinterpret_cast<uint32_t*>(&vb);
+              uint32_t* wc = reinterpret_cast<uint32_t*>(&vc);
+#pragma unroll
+              for (int qq = 0; qq < 4; ++qq) {
+                const float2 bb = unpack_bf16x2(wb[qq]), cc = unpack_bf16x2(wc[qq]);
+                const float b0 = cs[qq] * bb.x + sn[qq] * bb.y, b1 = -sn[qq] * bb.x + cs[qq] * bb.y;
+                const float c0 = cs[qq] * cc.x + sn[qq] * cc.y, c1 = -sn[qq] * cc.x + cs[qq] * cc.y;
+                range = fmaxf(range, fmaxf(fmaxf(fabsf(b0), fabsf(b1)), fmaxf(fabsf(c0), fabsf(c1))));
+                wb[qq] = pack_f16x2(b0, b1);
+                wc[qq] = pack_f16x2(c0, c1);
+              }
+              *reinterpret_cast<uint4*>(stg + off) = vb;
+              *reinterpret_cast<uint4*>(stg + C::TILE + off) = vc;
+            }
+          }
+          if (tb == TB - 1) {
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) s_carry[(s ^ 1) * 64 + 4 * pg + qq] = reduce_angle(ang[qq]);
+          }
+        }
+        // d X into the single fp16 buffer, once GEMM4 of the previous chunk has read it
+        if (k >= 1) ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_UFULL), (k - 1) & 1, s_abort));
+        if (!ab) {
+          const uint8_t* sx = sm + s * C::STAGE + 2 * C::TILE;
+          uint8_t* sdx = sm + C::OFF_DX;
+          const float dv = s_d[xt >> C::kLogR];
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const uint32_t off = sw128(xt, g);
+            uint4 v = *reinterpret_cast<const uint4*>(sx + off);
+            uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+              const float2 xx = unpack_bf16x2(w[qq]);
+              const float a0 = dv * xx.x, a1 = dv * xx.y;
+              range = fmaxf(range, fmaxf(fabsf(a0), fabsf(a1)));
+              w[qq] = pack_f16x2(a0, a1);
+            }
+            *reinterpret_cast<uint4*>(sdx + off) = v;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_XF + s));
         }
       }
-      if (lane == 0) s_scal[0] = ex2(ell_last);
+      cur_dt = nxt_dt;
+      cur_lam = nxt_lam;
+      qn_cur = qn_nxt;
+#pragma unroll
+      for (int u = 0; u < TPT; ++u) th_cur[u] = th_nxt[u];
     }
-    // theta for this thread's tokens and pairs (registers)
-    float th[TPT][4];
-    if (rot_thread) {
-#pragma unroll
-      for (int u = 0; u < TPT; ++u) {
-        const int t = t0 + tb * TPT + u;
-        if (t < T) {
-          const uint2 raw = *reinterpret_cast<const uint2*>(
-              p.theta + ((static_cast<size_t>(b) * T + t) * H + head) * K + 4 * pg);
-          const float2 a = unpack_bf16x2(raw.x), c = unpack_bf16x2(raw.y);
-          th[u][0] = a.x; th[u][1] = a.y; th[u][2] = c.x; th[u][3] = c.y;
-        } else {
-          th[u][0] = th[u][1] = th[u][2] = th[u][3] = 0.f;
-        }
-      }
+    if (range > kF16Max) atomicOr(p.status, kDevRange);
+    // ---------------------------------------------------------------- exit angle and token
+    bar_sync_or(kBarXf, kRole, ab);
+    if (!ab) {
+      if (p.phiT)
+        for (int k = xt; k < K; k += kRole)
+          p.phiT[static_cast<size_t>(bh) * K + k] = s_carry[(nchunks & 1) * 64 + k];
+      const size_t last = (seq0 + static_cast<size_t>(T - 1) * tok_stride);
+      if (p.prevBT)
+        for (int e = xt; e < R * NS; e += kRole)
+          p.prevBT[static_cast<size_t>(bh) * R * NS + e] = p.B[last * R * NS + e];
+      if (p.prevxT)
+        for (int e = xt; e < R * kP; e += kRole)
+          p.prevxT[static_cast<size_t>(bh) * R * kP + e] = p.x[last * R * kP + e];
     }
-    __syncthreads();
+  } else {
+    // ================================================================ epilogue
+    const int q = warp & 3;          // TMEM lane quarter of this warp
+    const int ew = warp - kWarpEpi;  // epilogue warp index 0..3
+    const int i = q * 32 + lane;     // TMEM lane = chunk row = state row
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const bool srow = i < NS;
+    const float* s_ell = misc + C::M_ELL;
+    const float* s_w = misc + C::M_W;
+    const float* s_gam = misc + C::M_GAM;
+    const float* s_el = misc + C::M_EL;
+    const float* s_elast = misc + C::M_ELAST;
+    float* s_hmax = misc + C::M_HMAX;
+    uint8_t* sHb = sm + C::OFF_H;
+    const size_t seq0 = static_cast<size_t>(b) * T * H + head;
 
-    // ------------------------------------------------------------ cumulative angle, rotation
-    float phl[TPT][4];
-    if (rot_thread) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float hv[kP];
+    // -------------------------------------------------------------- entry state
+    // H' = h0 + q_0 B~_{-1} X_{-1}^T: the stored previous token rotated by its own angle
+    // phi0, weighted by q_0 = (1 - lambda_0) dt_0 of this call's first token.
+    {
+      const float q0 = (1.f - __bfloat162float(p.lam[seq0])) * __bfloat162float(p.dt[seq0]);
+      float bt[R];
 #pragma unroll
-      for (int u = 0; u < TPT; ++u) {
-        const float d = s_dt[tb * TPT + u];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          acc[q] = fmaf(d, th[u][q], acc[q]);
-          phl[u][q] = acc[q];
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) s_scan[tb * K + 4 * pg + q] = acc[q];
-    }
-    __syncthreads();
-    ok = mbar_wait(bar_tma, ck & 1) && ok;
-    if (rot_thread) {
-      float base[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) base[q] = s_carry[(ck & 1) * 64 + 4 * pg + q];
-      for (int tb2 = 0; tb2 < tb; ++tb2)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) base[q] += s_scan[tb2 * K + 4 * pg + q];
-      const int nb = pg >> 3, c16 = pg & 7;
-#pragma unroll
-      for (int u = 0; u < TPT; ++u) {
-        float cs[4], sn[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) __sincosf(reduce_angle(base[q] + phl[u][q]), &sn[q], &cs[q]);
-        const int i = tb * TPT + u;
+      for (int r = 0; r < R; ++r) bt[r] = 0.f;
+      if (srow && p.prevB0) {
+        const int kk = i >> 1;
+        const float ph = p.phi0 ? p.phi0[static_cast<size_t>(bh) * K + kk] : 0.f;
+        float sn, cs;
+        sincosf(ph, &sn, &cs);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-          const uint32_t off = nb * 16384u + sw128(i * R + r, c16);
-          uint4 vb = *reinterpret_cast<const uint4*>(sm + C::OFF_B + off);
-          uint4 vc = *reinterpret_cast<const uint4*>(sm + C::OFF_C + off);
-          uint4 lb, lc;
-          uint32_t* wb = reinterpret_cast<uint32_t*>(&vb);
-          uint32_t* wc = reinterpret_cast<uint32_t*>(&vc);
-          uint32_t* wlb = reinterpret_cast<uint32_t*>(&lb);
-          uint32_t* wlc = reinterpret_cast<uint32_t*>(&lc);
+          const __nv_bfloat16* pb = p.prevB0 + (static_cast<size_t>(bh) * R + r) * NS + 2 * kk;
+          const float u = __bfloat162float(pb[0]), v = __bfloat162float(pb[1]);
+          bt[r] = (i & 1) ? (-sn * u + cs * v) : (cs * u + sn * v);
+        }
+      }
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float2 bb = unpack_bf16x2(wb[q]), cc = unpack_bf16x2(wc[q]);
-            split2(cs[q] * bb.x + sn[q] * bb.y, -sn[q] * bb.x + cs[q] * bb.y, wb[q], wlb[q]);
-            split2(cs[q] * cc.x + sn[q] * cc.y, -sn[q] * cc.x + cs[q] * cc.y, wc[q], wlc[q]);
+      for (int pp = 0; pp < kP; ++pp) {
+        float v = 0.f;
+        if (srow) {
+          if (p.h0) v = p.h0[(static_cast<size_t>(bh) * NS + i) * kP + pp];
+          if (p.prevx0) {
+            float f = 0.f;
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+              f = fmaf(bt[r], __bfloat162float(p.prevx0[(static_cast<size_t>(bh) * R + r) * kP + pp]), f);
+            v = fmaf(q0, f, v);
           }
-          *reinterpret_cast<uint4*>(sm + C::OFF_B + off) = vb;
-          *reinterpret_cast<uint4*>(sm + C::OFF_C + off) = vc;
-          *reinterpret_cast<uint4*>(sm + C::OFF_BL + off) = lb;
-          *reinterpret_cast<uint4*>(sm + C::OFF_CL + off) = lc;
         }
-      }
-      if (tb == TB - 1) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          s_carry[((ck + 1) & 1) * 64 + 4 * pg + q] = reduce_angle(base[q] + phl[TPT - 1][q]);
+        hv[pp] = v;
       }
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    if (__syncthreads_or(!ok)) break;
-
-    // ------------------------------------------------------------ GEMM1: S = C~ B~^T
-    // (C_hi + C_lo)(B_hi + B_lo)^T without the lo*lo term.
-    if (tid == 0) {
-      tc_fence_after();
+    // Scaled fp16 copy of the state as the K-major B operand of GEMM3 (row p, column n).
+    auto put_state = [&](float sig) {
+      if (srow) {
+        const uint32_t base = (i >> 6) * 8192u + (i & 7) * 2;
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        const uint32_t ko = (ks >> 2) * 16384u + (ks & 3) * 32u;
-        tc_mma_ss(tS, sdesc_sw128(sC + ko, 16, 1024), sdesc_sw128(sB + ko, 16, 1024), I_S, ks > 0);
-        tc_mma_ss(tS, sdesc_sw128(sC + ko, 16, 1024), sdesc_sw128(sBl + ko, 16, 1024), I_S, 1);
-        tc_mma_ss(tS, sdesc_sw128(sCl + ko, 16, 1024), sdesc_sw128(sB + ko, 16, 1024), I_S, 1);
+        for (int pp = 0; pp < kP; ++pp)
+          *reinterpret_cast<__half*>(sHb + base + sw128(pp, (i & 63) >> 3)) = __float2half_rn(sig * hv[pp]);
       }
-      tc_commit(bar_mma);
-    }
-    ok = mbar_wait(bar_mma, mma_count & 1) && ok;
-    ++mma_count;
-    tc_fence_after();
-
-    // ------------------------------------------------------------ mask (registers)
-    uint32_t pkh[32], pkl[32];  // this thread's 64 masked scores as bf16 (hi, lo) pairs
+    };
+    auto max_abs = [&]() {
+      float mx = 0.f;
+#pragma unroll
+      for (int pp = 0; pp < kP; ++pp) mx = fmaxf(mx, fabsf(hv[pp]));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      return mx;
+    };
+    bool ab = false;
+    float sig_cur;
     {
-      const int i = trow >> C::kLogR;
-      const float ell_i = s_ell[i], gam_i = s_gam[i];
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        uint32_t sv[32];
-        tmem_ld32(tS + lane_off + 64 * half + 32 * h2, sv);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float m2[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = 64 * half + 32 * h2 + c + e;
-            const int j = col >> C::kLogR;
-            float m = 0.f;
-            if (j < i) m = ex2(ell_i - s_ell[j]) * s_wgt[j];
-            else if (j == i) m = gam_i;
-            m2[e] = m * __uint_as_float(sv[c + e]);
-          }
-          split2(m2[0], m2[1], pkh[16 * h2 + c / 2], pkl[16 * h2 + c / 2]);
-        }
-      }
-    }
-    // Scale B~ rows by d_j (for GEMM4) and C~ rows by e^{l_i} (for GEMM3), in place:
-    // recombine hi + lo in fp32, scale, split again.
-    {
-      const int row = tid & 127;
-      const int i = row >> C::kLogR;
-      const float fb = s_dsc[i], fc = s_eL[i];
-      const int hh = tid >> 7;
-#pragma unroll
-      for (int cc = 0; cc < NB * 4; ++cc) {
-        const int chunk = hh * NB * 4 + cc;  // 0 .. NB*8-1
-        const uint32_t off = (chunk >> 3) * 16384u + sw128(row, chunk & 7);
-        uint4 vb = *reinterpret_cast<const uint4*>(sm + C::OFF_B + off);
-        uint4 vc = *reinterpret_cast<const uint4*>(sm + C::OFF_C + off);
-        uint4 lb = *reinterpret_cast<const uint4*>(sm + C::OFF_BL + off);
-        uint4 lc = *reinterpret_cast<const uint4*>(sm + C::OFF_CL + off);
-        uint32_t* wb = reinterpret_cast<uint32_t*>(&vb);
-        uint32_t* wc = reinterpret_cast<uint32_t*>(&vc);
-        uint32_t* wlb = reinterpret_cast<uint32_t*>(&lb);
-        uint32_t* wlc = reinterpret_cast<uint32_t*>(&lc);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 bh_ = unpack_bf16x2(wb[q]), bl_ = unpack_bf16x2(wlb[q]);
-          const float2 ch_ = unpack_bf16x2(wc[q]), cl_ = unpack_bf16x2(wlc[q]);
-          split2(fb * (bh_.x + bl_.x), fb * (bh_.y + bl_.y), wb[q], wlb[q]);
-          split2(fc * (ch_.x + cl_.x), fc * (ch_.y + cl_.y), wc[q], wlc[q]);
-        }
-        *reinterpret_cast<uint4*>(sm + C::OFF_B + off) = vb;
-        *reinterpret_cast<uint4*>(sm + C::OFF_C + off) = vc;
-        *reinterpret_cast<uint4*>(sm + C::OFF_BL + off) = lb;
-        *reinterpret_cast<uint4*>(sm + C::OFF_CL + off) = lc;
-      }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    if (__syncthreads_or(!ok)) break;
-
-    // ------------------------------------------------------------ GEMM3 + GEMM4
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        const uint32_t ka = (ks >> 2) * 16384u + (ks & 3) * 32u;
-        const uint32_t kh = (ks >> 2) * 8192u + (ks & 3) * 32u;
-        tc_mma_ss(tY, sdesc_sw128(sC + ka, 16, 1024), sdesc_sw128(sH + kh, 16, 1024), I_CH, ks > 0);
-        tc_mma_ss(tY, sdesc_sw128(sC + ka, 16, 1024), sdesc_sw128(sHl + kh, 16, 1024), I_CH, 1);
-        tc_mma_ss(tY, sdesc_sw128(sCl + ka, 16, 1024), sdesc_sw128(sH + kh, 16, 1024), I_CH, 1);
-      }
-#pragma unroll
-      for (int ks = 0; ks < kRows / 16; ++ks) {
-        const uint32_t kr = ks * 2048u;
-        tc_mma_ss(tU, sdesc_sw128(sB + kr, 16384, 1024), sdesc_sw128(sX + kr, 16384, 1024), I_U,
-                  ks > 0);
-        tc_mma_ss(tU, sdesc_sw128(sBl + kr, 16384, 1024), sdesc_sw128(sX + kr, 16384, 1024), I_U, 1);
-      }
-      tc_commit(bar_mma);
-    }
-    ok = mbar_wait(bar_mma, mma_count & 1) && ok;
-    ++mma_count;
-    tc_fence_after();
-
-    // P -> shared memory (K-major A operand of GEMM2, in B~'s hi and lo buffers)
-#pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8) {
-      const uint32_t off = half * 16384u + sw128(trow, c8);
-      *reinterpret_cast<uint4*>(sm + C::OFF_P + off) =
-          make_uint4(pkh[4 * c8], pkh[4 * c8 + 1], pkh[4 * c8 + 2], pkh[4 * c8 + 3]);
-      *reinterpret_cast<uint4*>(sm + C::OFF_PL + off) =
-          make_uint4(pkl[4 * c8], pkl[4 * c8 + 1], pkl[4 * c8 + 2], pkl[4 * c8 + 3]);
-    }
-    // state: H <- e^{l_last} H + U
-    if ((warp & 3) * 32 < NS) {
-      const float eLast = s_scal[0];
-      uint32_t hv[32], uv[32];
-      tmem_ld32(tHc + lane_off + 32 * half, hv);
-      tmem_ld32(tU + lane_off + 32 * half, uv);
-      tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        hv[j] = __float_as_uint(fmaf(eLast, __uint_as_float(hv[j]), __uint_as_float(uv[j])));
-      put_state(hv);
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    if (__syncthreads_or(!ok)) break;
-
-    // ------------------------------------------------------------ GEMM2: Y += (P_hi + P_lo) X
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int ks = 0; ks < kRows / 16; ++ks) {
-        const uint32_t ka = (ks >> 2) * 16384u + (ks & 3) * 32u;
-        const uint64_t bx = sdesc_sw128(sX + ks * 2048u, 16384, 1024);
-        tc_mma_ss(tY, sdesc_sw128(sP + ka, 16, 1024), bx, I_PX, 1);
-        tc_mma_ss(tY, sdesc_sw128(sPl + ka, 16, 1024), bx, I_PX, 1);
-      }
-      tc_commit(bar_mma);
-    }
-    ok = mbar_wait(bar_mma, mma_count & 1) && ok;
-    ++mma_count;
-    tc_fence_after();
-    if (tid == 0 && ok && ck + 1 < nchunks) {
+      const float mx = max_abs();
+      if (lane == 0) s_hmax[ew] = mx;
+      bar_sync_or(kBarEpi, kRole, false);
+      sig_cur = state_scale(fmaxf(fmaxf(s_hmax[0], s_hmax[1]), fmaxf(s_hmax[2], s_hmax[3])));
+      put_state(sig_cur);
       fence_proxy_async_smem();
-      issue_tma(ck + 1);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_STATE));
     }
 
-    // ------------------------------------------------------------ y
-    {
-      uint32_t yv[32];
-      tmem_ld32(tY + lane_off + 32 * half, yv);
-      tmem_ld_wait();
-      const int i = trow >> C::kLogR, r = trow & (R - 1);
-      const int t = t0 + i;
-      if (t < T) {
-        const size_t o = (((static_cast<size_t>(b) * T + t) * H + head) * R + r) * kP + 32 * half;
-        if (p.out_bf16) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) + o);
+    for (int k = 0; k < nchunks; ++k) {
+      const int s = k & 1;
+      const int t0 = k * CT;
+      const uint32_t tS = tmem + TM_S + 128u * s;
+      const int ti = i >> C::kLogR;
+      // ---------------------------------------------------------- mask: S -> P (bf16 hi/lo)
+      // (the transform's arrival on B_XF publishes this chunk's decay sums and weights)
+      ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_XF + s), (k >> 1) & 1, s_abort));
+      ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_SFULL + s), (k >> 1) & 1, s_abort));
+      const float el_i = ab ? 0.f : s_el[s * 128 + ti];
+      if (!ab) {
+        tc_fence_after();
+        const float ell_i = s_ell[s * 128 + ti], gam_i = s_gam[s * 128 + ti];
+        const int whi = (q * 32 + 31) >> C::kLogR;  // last token among this warp's rows
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dst[q] = make_uint4(
-                pack_bf16x2(__uint_as_float(yv[8 * q + 0]), __uint_as_float(yv[8 * q + 1])),
-                pack_bf16x2(__uint_as_float(yv[8 * q + 2]), __uint_as_float(yv[8 * q + 3])),
-                pack_bf16x2(__uint_as_float(yv[8 * q + 4]), __uint_as_float(yv[8 * q + 5])),
-                pack_bf16x2(__uint_as_float(yv[8 * q + 6]), __uint_as_float(yv[8 * q + 7])));
-        } else {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.y) + o);
+        for (int blk = 0; blk < 4; ++blk) {
+          uint32_t hi[16], lo[16];
+          if (((32 * blk) >> C::kLogR) > whi) {
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(__uint_as_float(yv[4 * q]), __uint_as_float(yv[4 * q + 1]),
-                                 __uint_as_float(yv[4 * q + 2]), __uint_as_float(yv[4 * q + 3]));
+            for (int c = 0; c < 16; ++c) hi[c] = lo[c] = 0u;
+          } else {
+            uint32_t sv[32];
+            tmem_ld32(tS + lane_off + 32u * blk, sv);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              float m2[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int tj = (32 * blk + c + e) >> C::kLogR;
+                float m = 0.f;
+                if (tj < ti) m = ex2(ell_i - s_ell[s * 128 + tj]) * s_w[s * 128 + tj];
+                else if (tj == ti) m = gam_i;
+                m2[e] = m * __uint_as_float(sv[c + e]);
+              }
+              split2(m2[0], m2[1], hi[c >> 1], lo[c >> 1]);
+            }
+          }
+          tmem_st16(tS + lane_off + 32u * blk, hi);
+          tmem_st16(tS + lane_off + 32u * blk + 16u, lo);
         }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_PFULL + s));
       }
+      // ---------------------------------------------------------- state: H <- e^{L} H + U
+      ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_UFULL), k & 1, s_abort));
+      ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_HFREE), k & 1, s_abort));
+      float mx = 0.f;
+      if (!ab) {
+        tc_fence_after();
+        if (q * 32 < NS) {  // warp-uniform: this warp owns state rows
+          const float eL = s_elast[s];
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t uv[32];
+            tmem_ld32(tmem + TM_U + lane_off + 32u * half, uv);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) hv[32 * half + j] = fmaf(eL, hv[32 * half + j], __uint_as_float(uv[j]));
+          }
+        }
+        mx = max_abs();
+        if (lane == 0) s_hmax[(s ^ 1) * 4 + ew] = mx;
+      }
+      if (bar_sync_or(kBarEpi, kRole, ab)) { ab = true; break; }
+      const float sig_next = state_scale(fmaxf(fmaxf(s_hmax[(s ^ 1) * 4 + 0], s_hmax[(s ^ 1) * 4 + 1]),
+                                               fmaxf(s_hmax[(s ^ 1) * 4 + 2], s_hmax[(s ^ 1) * 4 + 3])));
+      put_state(sig_next);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_STATE));
+      // ---------------------------------------------------------- y = P X + e^{l} C~ H
+      ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_YFULL), k & 1, s_abort));
+      if (!ab) {
+        tc_fence_after();
+        const float f = el_i / sig_cur;
+        const int r = i & (R - 1);
+        const int t = t0 + ti;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t a[32], c[32];
+          tmem_ld32(tmem + TM_YIN + lane_off + 32u * half, a);
+          tmem_ld32(tmem + TM_YOFF + lane_off + 32u * half, c);
+          tmem_ld_wait();
+          if (t < T) {
+            const size_t o = ((seq0 + static_cast<size_t>(t) * H) * R + r) * kP + 32 * half;
+            if (p.out_bf16) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) + o);
+#pragma unroll
+              for (int qq = 0; qq < 4; ++qq) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int j = 8 * qq + 2 * e;
+                  w[e] = pack_bf16x2(fmaf(f, __uint_as_float(c[j]), __uint_as_float(a[j])),
+                                     fmaf(f, __uint_as_float(c[j + 1]), __uint_as_float(a[j + 1])));
+                }
+                dst[qq] = make_uint4(w[0], w[1], w[2], w[3]);
+              }
+            } else {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.y) + o);
+#pragma unroll
+              for (int qq = 0; qq < 8; ++qq) {
+                float v[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  v[e] = fmaf(f, __uint_as_float(c[4 * qq + e]), __uint_as_float(a[4 * qq + e]));
+                dst[qq] = make_float4(v[0], v[1], v[2], v[3]);
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_YFREE));
+      }
+      sig_cur = sig_next;
     }
-    tc_fence_before();
-    if (__syncthreads_or(!ok)) break;
+    // ---------------------------------------------------------------- exit state
+    if (!ab && p.hT && srow) {
+      float4* dst = reinterpret_cast<float4*>(p.hT + (static_cast<size_t>(bh) * NS + i) * kP);
+#pragma unroll
+      for (int qq = 0; qq < kP / 4; ++qq)
+        dst[qq] = make_float4(hv[4 * qq], hv[4 * qq + 1], hv[4 * qq + 2], hv[4 * qq + 3]);
+    }
   }
 
-  if (!ok) {
-    if (tid == 0) atomicOr(p.status, kDevTimeout);
-  } else {
-    // ------------------------------------------------------------ exit state
-    if (p.hT && (warp & 3) * 32 < NS) {
-      uint32_t hv[32];
-      tmem_ld32(tHc + lane_off + 32 * half, hv);
-      tmem_ld_wait();
-      float4* dst =
-          reinterpret_cast<float4*>(p.hT + (static_cast<size_t>(bh) * NS + trow) * kP + 32 * half);
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        dst[q] = make_float4(__uint_as_float(hv[4 * q]), __uint_as_float(hv[4 * q + 1]),
-                             __uint_as_float(hv[4 * q + 2]), __uint_as_float(hv[4 * q + 3]));
-    }
-    if (p.phiT)
-      for (int k = tid; k < K; k += kThreads)
-        p.phiT[static_cast<size_t>(bh) * K + k] = s_carry[(nchunks & 1) * 64 + k];
-    if (p.prevBT)
-      for (int e = tid; e < R * NS; e += kThreads)
-        p.prevBT[static_cast<size_t>(bh) * R * NS + e] =
-            T > 0 ? p.B[((static_cast<size_t>(b) * T + T - 1) * H + head) * R * NS + e]
-                  : (p.prevB0 ? p.prevB0[static_cast<size_t>(bh) * R * NS + e] : __float2bfloat16_rn(0.f));
-    if (p.prevxT)
-      for (int e = tid; e < R * kP; e += kThreads)
-        p.prevxT[static_cast<size_t>(bh) * R * kP + e] =
-            T > 0 ? p.x[((static_cast<size_t>(b) * T + T - 1) * H + head) * R * kP + e]
-                  : (p.prevx0 ? p.prevx0[static_cast<size_t>(bh) * R * kP + e] : __float2bfloat16_rn(0.f));
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (tid == 0 && *s_abort) atomicOr(p.status, kDevTimeout);
+  if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ---------------------------------------------------------------- host side

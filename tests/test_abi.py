@@ -14,7 +14,7 @@ from state_space_sequence_trapezoidal_b300 import M3Dims, M3State
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
-OK, ARG, SHAPE, DTYPE, ALIGN, CUDA, TIMEOUT, UNSUP, WS = range(9)
+OK, ARG, SHAPE, DTYPE, ALIGN, CUDA, TIMEOUT, UNSUP, WS, RANGE = range(10)
 
 
 def declared_functions():
@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported():
 
 def test_status_strings():
     lib = m3.load()
-    for s in range(9):
+    for s in range(10):
         assert lib.m3_status_str(s)
     assert lib.m3_status_str(99) == b"unknown status"
 
