@@ -18,27 +18,31 @@
 // which carries the trapezoid's previous-token term across the boundary.
 // B~, C~ are B, C rotated by the cumulative angle (Proposition 3).
 //
-// Kernel design: one CTA per (batch row, head) sequence, 10 warps with fixed roles,
+// Kernel design: one CTA per (batch row, head) sequence, 14 warps with fixed roles;
 // chunks flow through a two-stage pipeline so that loads, CUDA-core work and
 // tensor-core work of neighbouring chunks overlap:
-//   warp 0      TMA producer: raw bf16 tiles of B, C and X (128-byte swizzle) into
-//               one of two stages.
-//   warp 1      MMA issuer (one thread): GEMM1, GEMM4, GEMM3, GEMM2 per chunk.
-//   warps 2-5   transform: discretisation (decay log-sums, trapezoid weights), the
-//               cumulative angle, rotation of B and C in place to fp16, and the
-//               d-scaled copy of X in fp16.  theta, dt and lambda are prefetched
-//               into registers one chunk ahead.
-//   warps 6-9   epilogue (one thread per TMEM lane): mask the scores in TMEM into
-//               bf16 hi/lo pairs (GEMM2 reads them from TMEM), advance the fp32
-//               state (kept in registers) and write its scaled fp16 copy for
-//               GEMM3, and write y.
+//   warp 0       TMA producer: raw bf16 tiles of B, C and X (128-byte swizzle) into
+//                one of two stages.
+//   warp 1       MMA issuer (one thread): GEMM1, GEMM4, GEMM3, GEMM2 per chunk.
+//   warps 2-9    transform: discretisation (decay log-sums, trapezoid weights), the
+//                cumulative angle, rotation of B and C in place to fp16, and the
+//                d-scaled copy of X in fp16.  theta, dt and lambda are prefetched
+//                into registers one chunk ahead.
+//   warps 10-13  epilogue (one thread per TMEM lane): mask the scores in TMEM into
+//                bf16 hi/lo pairs (GEMM2 reads them from TMEM), advance the fp32
+//                state (kept in TMEM) and write its scaled fp16 copy for GEMM3, and
+//                write y.
+// The decay factor of a score below the diagonal 32x32 block is split as
+// 2^{l_i - l_ref} * 2^{l_ref - l_j} with l_ref the decay sum of the block's last
+// column: both factors are at most 1, so nothing overflows, and the per-column
+// factor (times w_j) is computed once per chunk instead of once per score.
 // Operand precision: B~, C~, the state copy and d X are fp16 (11 significant
 // bits; the state copy carries a per-chunk power-of-two scale), the masked scores
 // are bf16 hi + lo (about 16 bits, full fp32 range), X is the exact bf16 input;
 // every product accumulates in fp32 in TMEM.  The measured error of this scheme
 // is about 0.6-0.8% of the output RMS at the benchmark shapes.
 // TMEM (512 columns): [0,256) two score buffers, [256,320) C~H, [320,384) PX,
-// [384,448) the chunk's state increment U.
+// [384,448) the chunk's state increment U, [448,512) the fp32 state H.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -54,12 +58,13 @@ namespace {
 
 constexpr int kRows = 128;  // (token, rank) rows per chunk
 constexpr int kP = 64;      // head dimension handled by this kernel
-constexpr int kThreads = 320;
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpXf = 2, kWarpEpi = 6;
-constexpr int kRole = 128;  // threads of the transform and of the epilogue role
-constexpr uint32_t kBarXf = 1, kBarEpi = 2;  // named barrier ids
+constexpr int kThreads = 576;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpXf = 2, kWarpMask = 10, kWarpSy = 14;
+constexpr int kXf = 256;   // transform threads
+constexpr int kEpi = 128;  // threads of each epilogue group (one per TMEM lane)
+constexpr uint32_t kBarXf = 1, kBarSy = 2;  // named barrier ids
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t TM_S = 0, TM_YOFF = 256, TM_YIN = 320, TM_U = 384;
+constexpr uint32_t TM_S = 0, TM_YOFF = 256, TM_YIN = 320, TM_U = 384, TM_H = 448;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kTwoPi = 6.283185307179586f;
 constexpr float kInvTwoPi = 0.15915494309189535f;
@@ -67,23 +72,27 @@ constexpr float kF16Max = 65504.f;
 
 // mbarriers
 enum {
-  B_FULL = 0,    // [2] TMA tiles of a stage landed
-  B_SFREE = 2,   // [2] stage and score buffer free again (commit after GEMM2)
-  B_XF = 4,      // [2] transform finished a chunk (4 warp arrivals)
-  B_SFULL = 6,   // [2] scores in TMEM (commit after GEMM1)
-  B_PFULL = 8,   // [2] masked scores written back (4 warp arrivals)
-  B_UFULL = 10,  // state increment U in TMEM (commit after GEMM4)
-  B_STATE = 11,  // state advanced: U read, next h^T copy in shared memory (4 arrivals)
-  B_HFREE = 12,  // GEMM3 finished reading h^T (commit)
-  B_YFULL = 13,  // GEMM2 finished: both output accumulators complete (commit)
-  B_YFREE = 14,  // epilogue read both output accumulators (4 arrivals)
-  NUM_BARS = 15
+  B_FULL = 0,     // [2] TMA tiles of B and C landed
+  B_FULLX = 2,    // [2] TMA tile of X landed
+  B_BCFREE = 4,   // [2] B~, C~ of a stage no longer read (commit after GEMM3)
+  B_XFREE = 6,    // [2] X of a stage and the score buffer free again (commit after GEMM2)
+  B_XF = 8,       // [2] transform finished a chunk (one arrival per transform warp)
+  B_SFULL = 10,   // [2] scores in TMEM (commit after GEMM1)
+  B_PFULL = 12,   // [2] masked scores written back (one arrival per epilogue warp)
+  B_UFULL = 14,   // state increment U in TMEM (commit after GEMM4)
+  B_STATE = 15,   // state advanced: U read, next fp16 state copy in shared memory
+  B_HFREE = 16,   // GEMM3 finished reading the fp16 state copy (commit)
+  B_YFULL = 17,   // GEMM2 finished: both output accumulators complete (commit)
+  B_YFREE = 18,   // epilogue read both output accumulators
+  B_MFREE = 19,   // [2] both epilogue groups done with a chunk's decay sums and weights
+  NUM_BARS = 21
 };
 
 struct TcParams {
   CUtensorMap tmB;  // B [B][T][H][R][N] bf16, box {64, R, 1, CT, 1}
   CUtensorMap tmC;  // C, same
   CUtensorMap tmX;  // x [B][T][H][R][P] bf16, box {64, R, 1, CT, 1}
+  CUtensorMap tmY;  // y [B][T][H][R][P] fp32 (box {32, R, 1, 32/R, 1}) or bf16 (box {64, ...})
   const __nv_bfloat16* x;
   const __nv_bfloat16* B;
   const __nv_bfloat16* dt;
@@ -106,32 +115,37 @@ struct TcParams {
 
 template <int NS, int R>
 struct Cfg {
-  static constexpr int CT = kRows / R;   // tokens per chunk
-  static constexpr int NB = NS / 64;     // 64-wide blocks of the state dimension
-  static constexpr int K = NS / 2;       // rotation pairs
-  static constexpr int PG = K / 4;       // 16-byte groups (4 pairs) per row
-  static constexpr int TB = kRole / PG;  // token blocks of the rotation
-  static constexpr int TPT = CT / TB;    // tokens per rotation thread
+  static constexpr int CT = kRows / R;  // tokens per chunk
+  static constexpr int NB = NS / 64;    // 64-wide blocks of the state dimension
+  static constexpr int K = NS / 2;      // rotation pairs
+  static constexpr int PG = K / 4;      // 16-byte groups (4 pairs) per row
+  static constexpr int TBX = kXf / PG;  // thread groups per pair group
+  static constexpr int TB = TBX < CT ? TBX : CT;  // token blocks of the rotation
+  static constexpr int RS = TBX / TB;             // rank rows split over RS threads
+  static constexpr int TPT = CT / TB;             // tokens per rotation thread
+  static constexpr int TPB = 32 / R;              // tokens per 32-column score block
   static constexpr int kLogR = R == 1 ? 0 : R == 2 ? 1 : R == 4 ? 2 : 3;
   // shared memory (bytes from a 1024-aligned base)
-  static constexpr uint32_t TILE = NB * 16384;        // 128 rows x NS, bf16 or fp16
+  static constexpr uint32_t TILE = NB * 16384;         // 128 rows x NS, bf16 or fp16
   static constexpr uint32_t STAGE = 2 * TILE + 16384;  // B~, C~, X
   static constexpr uint32_t OFF_DX = 2 * STAGE;        // d X, fp16 [128 rows][64]
-  static constexpr uint32_t OFF_H = OFF_DX + 16384;    // h^T, fp16 [NB][64 p][64 n]
-  static constexpr uint32_t OFF_MISC = OFF_H + NB * 8192;
+  static constexpr uint32_t OFF_H = OFF_DX + 16384;    // state copy, fp16 [NS rows n][64 p]
+  static constexpr uint32_t OFF_Y = OFF_H + NS * 128;   // [4 warps][32 rows][128 B] y staging
+  static constexpr uint32_t OFF_MISC = OFF_Y + 4 * 4096;
   // misc floats
-  static constexpr int M_ELL = 0;             // [2][128] decay log2-sums
-  static constexpr int M_W = 256;             // [2][128] trapezoid column weights
-  static constexpr int M_GAM = 512;           // [2][128] diagonal weights
-  static constexpr int M_EL = 768;            // [2][128] 2^{l}
-  static constexpr int M_ELAST = 1024;        // [2] 2^{l_last}
-  static constexpr int M_D = 1028;            // [128] d_j
-  static constexpr int M_DT = 1156;           // [128] dt
-  static constexpr int M_Q = 1284;            // [129] q, then q of the next chunk's first token
-  static constexpr int M_WSUM = 1416;         // [4] warp totals of the log2-decay scan
-  static constexpr int M_HMAX = 1420;         // [2][4] per-warp max |h|
-  static constexpr int M_CARRY = 1428;        // [2][64] angle carried into a chunk
-  static constexpr int M_SCAN = 1556;         // [TB][K] angle partial sums
+  static constexpr int M_ELL = 0;       // [2][128] decay log2-sums
+  static constexpr int M_W = 256;       // [2][128] trapezoid column weights
+  static constexpr int M_GAM = 512;     // [2][128] diagonal weights
+  static constexpr int M_EL = 768;      // [2][128] 2^{l}
+  static constexpr int M_G = 1024;      // [2][128] 2^{l_ref - l_j} w_j
+  static constexpr int M_ELAST = 1280;  // [2] 2^{l_last}
+  static constexpr int M_D = 1284;      // [128] d_j
+  static constexpr int M_DT = 1412;     // [128] dt
+  static constexpr int M_Q = 1540;      // [129] q, then q of the next chunk's first token
+  static constexpr int M_WSUM = 1672;   // [8] warp totals of the log2-decay scan
+  static constexpr int M_HMAX = 1680;   // [2][4] per-warp max |h|
+  static constexpr int M_CARRY = 1688;  // [2][64] angle carried into a chunk
+  static constexpr int M_SCAN = 1816;   // [TB][K] angle partial sums
   static constexpr int M_END = M_SCAN + TB * K;
   static constexpr uint32_t OFF_BAR = OFF_MISC + ((M_END * 4 + 15) / 16) * 16;
   static constexpr uint32_t OFF_HOLD = OFF_BAR + NUM_BARS * 8;  // TMEM base, abort flag
@@ -139,8 +153,8 @@ struct Cfg {
   static constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
   static_assert(kRows % R == 0, "R must divide 128");
   static_assert(NS == 64 || NS == 128, "N must be 64 or 128");
-  static_assert(TB * TPT == CT, "token split");
-  static_assert(CT <= kRole, "one discretisation thread per token");
+  static_assert(TB * TPT == CT && TB * RS == TBX && R % RS == 0, "rotation split");
+  static_assert(CT <= kXf, "one discretisation thread per token");
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory");
 };
 
@@ -153,10 +167,10 @@ __device__ __forceinline__ float reduce_angle(float a) {
 }
 
 // v = hi + lo with hi = bf16(v) and lo = bf16(v - hi): about 16 significant bits.
-__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+__device__ __forceinline__ void split2(float2 v, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
+  const float2 r = __fadd2_rn(v, make_float2(-__low2float(h), -__high2float(h)));
+  const __nv_bfloat162 l = __floats2bfloat162_rn(r.x, r.y);
   hi = *reinterpret_cast<const uint32_t*>(&h);
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
@@ -175,6 +189,7 @@ template <int NS, int R>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p) {
   using C = Cfg<NS, R>;
   constexpr int CT = C::CT, NB = C::NB, K = C::K, PG = C::PG, TB = C::TB, TPT = C::TPT;
+  constexpr int RS = C::RS, TPB = C::TPB;
   constexpr int KS = NS / 16;  // k-steps over the state dimension
 
   extern __shared__ uint8_t smem_raw[];
@@ -193,14 +208,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   const float A2 = p.A[head] * kLog2e;
 
   if (tid == 0) {
-    const int counts[NUM_BARS] = {1, 1, 1, 1, 4, 4, 1, 1, 4, 4, 1, 4, 1, 1, 4};
-    for (int i = 0; i < NUM_BARS; ++i) mbar_init(bar(i), counts[i]);
+    constexpr uint32_t nxw = kXf / 32, nep = kEpi / 32;  // arrivals: one per warp of a role
+#pragma unroll
+    for (int i = 0; i < NUM_BARS; ++i) {
+      const bool xf = i == B_XF || i == B_XF + 1;
+      const bool ep = i == B_PFULL || i == B_PFULL + 1 || i == B_STATE || i == B_YFREE;
+      const bool mf = i == B_MFREE || i == B_MFREE + 1;
+      mbar_init(bar(i), xf ? nxw : (ep ? nep : (mf ? 2 * nep : 1u)));
+    }
     *s_abort = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
     tma_prefetch_desc(&p.tmB);
     tma_prefetch_desc(&p.tmC);
     tma_prefetch_desc(&p.tmX);
+    tma_prefetch_desc(&p.tmY);
   }
   if (warp == kWarpMma) {
     tmem_alloc(smem_u32(s_tmem), kTmemCols);
@@ -214,29 +236,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   if (warp == kWarpTma) {
     // ================================================================ TMA producer
     if (lane == 0) {
-      int issued[2] = {-1, -1};
+      int issued[2] = {-1, -1}, issuedx[2] = {-1, -1};
       for (int k = 0; k < nchunks; ++k) {
         const int s = k & 1;
-        if (k >= 2 && !mbar_wait_abortable(bar(B_SFREE + s), ((k >> 1) - 1) & 1, s_abort)) break;
         const uint32_t st = sbase + s * C::STAGE;
-        mbar_arrive_expect_tx(bar(B_FULL + s), C::STAGE);
+        // B and C of chunk k once GEMM3 of chunk k - 2 has finished with this stage
+        if (k >= 2 && !mbar_wait_abortable(bar(B_BCFREE + s), ((k >> 1) - 1) & 1, s_abort)) break;
+        mbar_arrive_expect_tx(bar(B_FULL + s), 2 * C::TILE);
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
           tma_load_5d(st + nb * 16384, &p.tmB, bar(B_FULL + s), 64 * nb, 0, head, k * CT, b);
           tma_load_5d(st + C::TILE + nb * 16384, &p.tmC, bar(B_FULL + s), 64 * nb, 0, head, k * CT, b);
         }
-        tma_load_5d(st + 2 * C::TILE, &p.tmX, bar(B_FULL + s), 0, 0, head, k * CT, b);
         issued[s] = k;
+        // X of chunk k once GEMM2 of chunk k - 2 has finished with it
+        if (k >= 2 && !mbar_wait_abortable(bar(B_XFREE + s), ((k >> 1) - 1) & 1, s_abort)) break;
+        mbar_arrive_expect_tx(bar(B_FULLX + s), 16384);
+        tma_load_5d(st + 2 * C::TILE, &p.tmX, bar(B_FULLX + s), 0, 0, head, k * CT, b);
+        issuedx[s] = k;
       }
       // no copy may still be in flight when the CTA exits
-      for (int s = 0; s < 2; ++s)
+      for (int s = 0; s < 2; ++s) {
         if (issued[s] >= 0) mbar_wait(bar(B_FULL + s), (issued[s] >> 1) & 1);
+        if (issuedx[s] >= 0) mbar_wait(bar(B_FULLX + s), (issuedx[s] >> 1) & 1);
+      }
     }
   } else if (warp == kWarpMma) {
     // ================================================================ MMA issuer
     if (lane == 0) {
       constexpr uint32_t I_S = idesc_f16(128, 128, 0, 0);   // S = C~ B~^T
-      constexpr uint32_t I_CH = idesc_f16(128, 64, 0, 0);   // Y_off = C~ H
+      constexpr uint32_t I_CH = idesc_f16(128, 64, 0, 1);   // Y_off = C~ H  (H row-major)
       constexpr uint32_t I_U = idesc_f16(128, 64, 1, 1);    // U = B~^T (d X)
       constexpr uint32_t I_PX = idesc_bf16(128, 64, 0, 1);  // Y_in = P X
       const uint32_t sDX = sbase + C::OFF_DX, sH = sbase + C::OFF_H;
@@ -248,7 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const uint32_t sB = st, sC = st + C::TILE, sX = st + 2 * C::TILE;
         const uint32_t tS = tmem + TM_S + 128u * s;
         if (!mbar_wait_abortable(bar(B_XF + s), (k >> 1) & 1, s_abort)) break;
-        if (k >= 2 && !mbar_wait_abortable(bar(B_SFREE + s), ((k >> 1) - 1) & 1, s_abort)) break;
+        // the score buffer of this parity is free once GEMM2 of chunk k - 2 has read it
+        if (k >= 2 && !mbar_wait_abortable(bar(B_XFREE + s), ((k >> 1) - 1) & 1, s_abort)) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
@@ -274,13 +304,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
           const uint32_t ka = (ks >> 2) * 16384u + (ks & 3) * 32u;
-          const uint32_t kh = (ks >> 2) * 8192u + (ks & 3) * 32u;
-          tc_mma_ss(tmem + TM_YOFF, sdesc_sw128(sC + ka, 16, 1024), sdesc_sw128(sH + kh, 16, 1024), I_CH,
-                    ks > 0);
+          tc_mma_ss(tmem + TM_YOFF, sdesc_sw128(sC + ka, 16, 1024),
+                    sdesc_sw128(sH + ks * 2048u, NS * 128u, 1024), I_CH, ks > 0);
         }
         tc_commit(bar(B_HFREE));
-        last_bar = B_HFREE;
-        last_par = k & 1;
+        tc_commit(bar(B_BCFREE + s));
+        last_bar = B_BCFREE + s;
+        last_par = (k >> 1) & 1;
         if (!mbar_wait_abortable(bar(B_PFULL + s), (k >> 1) & 1, s_abort)) break;
         tc_fence_after();
         // masked scores as A from TMEM: per 32-column block, 16 columns of bf16 hi pairs
@@ -296,22 +326,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                         sdesc_sw128(sX + j0 * 128u, 16384, 1024), I_PX, (blk | part | sub) != 0);
             }
         tc_commit(bar(B_YFULL));
-        tc_commit(bar(B_SFREE + s));
-        last_bar = B_SFREE + s;
+        tc_commit(bar(B_XFREE + s));
+        last_bar = B_XFREE + s;
         last_par = (k >> 1) & 1;
       }
       // every MMA must be complete before the TMEM is released (the last commit tracks all)
       if (last_bar >= 0) mbar_wait(bar(last_bar), last_par);
     }
-  } else if (warp < kWarpEpi) {
+  } else if (warp < kWarpMask) {
     // ================================================================ transform
-    const int xt = tid - kWarpXf * 32;  // 0..127
+    const int xt = tid - kWarpXf * 32;  // 0..255
     const int xw = xt >> 5;
-    const int pg = xt % PG, tb = xt / PG;
+    const int pg = xt % PG, tb = (xt / PG) % TB, rs = xt / (PG * TB);
     float* s_ell = misc + C::M_ELL;
     float* s_w = misc + C::M_W;
     float* s_gam = misc + C::M_GAM;
     float* s_el = misc + C::M_EL;
+    float* s_g = misc + C::M_G;
     float* s_elast = misc + C::M_ELAST;
     float* s_d = misc + C::M_D;
     float* s_dt = misc + C::M_DT;
@@ -321,51 +352,56 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     float* s_scan = misc + C::M_SCAN;
     const size_t tok_stride = static_cast<size_t>(H);
     const size_t seq0 = static_cast<size_t>(b) * T * H + head;  // token 0 of this sequence
+    const uint16_t* dt16 = reinterpret_cast<const uint16_t*>(p.dt);
+    const uint16_t* lam16 = reinterpret_cast<const uint16_t*>(p.lam);
+    auto bf = [](uint32_t bits16) { return __uint_as_float(bits16 << 16); };
 
-    auto load_tok = [&](int kk, float& d, float& l) {
-      const int t = kk * CT + xt;
-      d = 0.f;
-      l = 0.f;
-      if (xt < CT && t < T) {
-        d = __bfloat162float(p.dt[seq0 + t * tok_stride]);
-        l = __bfloat162float(p.lam[seq0 + t * tok_stride]);
-      }
+    // Prefetch loads are unconditional, from token indices clamped into the sequence,
+    // and no instruction touches a loaded register until the next chunk: a guarded load
+    // would be followed by a select that waits for the data.  Tokens past the end are
+    // zeroed at use (their dt is 0, which also cancels their theta).
+    auto tok_of = [&](int kk) { return kk * CT + xt; };
+    auto clampT = [&](int t) { return t < T ? t : T - 1; };
+    auto load_tok = [&](int kk, uint16_t& d, uint16_t& l) {
+      const size_t o = seq0 + static_cast<size_t>(clampT(tok_of(kk))) * tok_stride;
+      d = dt16[o];
+      l = lam16[o];
     };
-    auto load_q = [&](int kk) -> float {
-      const int t = kk * CT;
-      if (xt != 0 || t >= T) return 0.f;
-      return (1.f - __bfloat162float(p.lam[seq0 + t * tok_stride])) *
-             __bfloat162float(p.dt[seq0 + t * tok_stride]);
+    auto load_q = [&](int kk, uint16_t& d, uint16_t& l) {  // chunk kk's first token
+      const size_t o = seq0 + static_cast<size_t>(clampT(kk * CT)) * tok_stride;
+      d = dt16[o];
+      l = lam16[o];
     };
     auto load_th = [&](int kk, uint2 (&th)[TPT]) {
 #pragma unroll
       for (int u = 0; u < TPT; ++u) {
-        const int t = kk * CT + tb * TPT + u;
-        th[u] = make_uint2(0u, 0u);
-        if (t < T)
-          th[u] = *reinterpret_cast<const uint2*>(p.theta + (seq0 + t * tok_stride) * K + 4 * pg);
+        const int t = clampT(kk * CT + tb * TPT + u);
+        th[u] = *reinterpret_cast<const uint2*>(p.theta + (seq0 + t * tok_stride) * K + 4 * pg);
       }
     };
 
-    float cur_dt, cur_lam, nxt_dt = 0.f, nxt_lam = 0.f;
+    uint16_t dt_cur, lam_cur, dt_nxt = 0, lam_nxt = 0, qd_cur, ql_cur, qd_nxt = 0, ql_nxt = 0;
+    load_tok(0, dt_cur, lam_cur);
+    load_q(1, qd_cur, ql_cur);
     uint2 th_cur[TPT], th_nxt[TPT];
-    load_tok(0, cur_dt, cur_lam);
-    float qn_cur = load_q(1), qn_nxt = 0.f;
     load_th(0, th_cur);
 #pragma unroll
     for (int u = 0; u < TPT; ++u) th_nxt[u] = make_uint2(0u, 0u);
-    for (int k = xt; k < K; k += kRole) s_carry[k] = reduce_angle(p.phi0 ? p.phi0[static_cast<size_t>(bh) * K + k] : 0.f);
+    for (int k = xt; k < K; k += kXf)
+      s_carry[k] = reduce_angle(p.phi0 ? p.phi0[static_cast<size_t>(bh) * K + k] : 0.f);
     float range = 0.f;  // largest |value| converted to fp16
     bool ab = false;
 
     for (int k = 0; k < nchunks; ++k) {
       const int s = k & 1;
       if (k + 1 < nchunks) {
-        load_tok(k + 1, nxt_dt, nxt_lam);
+        load_tok(k + 1, dt_nxt, lam_nxt);
         load_th(k + 1, th_nxt);
       }
-      qn_nxt = load_q(k + 2);
+      load_q(k + 2, qd_nxt, ql_nxt);
       // ---------------------------------------------------------- step A: decay scan
+      const bool tok_ok = xt < CT && tok_of(k) < T;
+      const float cur_dt = tok_ok ? bf(dt_cur) : 0.f, cur_lam = tok_ok ? bf(lam_cur) : 0.f;
       const float a2 = cur_dt * A2;
       const float gam = cur_lam * cur_dt;
       float incl = a2;
@@ -379,108 +415,127 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         s_q[xt] = (1.f - cur_lam) * cur_dt;
         s_dt[xt] = cur_dt;
       }
-      if (xt == 0) s_q[CT] = qn_cur;
-      // the epilogue must be done with this misc slot (chunk k - 2)
-      if (k >= 2) ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_PFULL + s), ((k >> 1) - 1) & 1, s_abort));
-      if (bar_sync_or(kBarXf, kRole, ab)) { ab = true; break; }
+      if (xt == 0) s_q[CT] = (k + 1) * CT < T ? (1.f - bf(ql_cur)) * bf(qd_cur) : 0.f;
+      // both epilogue groups must be done with this misc slot (chunk k - 2)
+      if (k >= 2)
+        ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_MFREE + s), ((k >> 1) - 1) & 1, s_abort));
+      if (bar_sync_or(kBarXf, kXf, ab)) { ab = true; break; }
       // ---------------------------------------------------------- step B: weights, angle partials
       {
         float ell = incl, ltot = 0.f;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
+        for (int w = 0; w < kXf / 32; ++w) {
           const float v = s_wsum[w];
           ltot += v;
           if (w < xw) ell += v;
         }
+        const float w = gam + s_q[xt + 1 < CT + 1 ? xt + 1 : CT];
+        // decay sum of the last token of this token's 32-column score block
+        const float ell_ref = __shfl_sync(0xffffffffu, ell, lane | (TPB - 1));
         if (xt < CT) {
-          const float w = gam + s_q[xt + 1];
           s_ell[s * 128 + xt] = ell;
           s_w[s * 128 + xt] = w;
           s_gam[s * 128 + xt] = gam;
           s_el[s * 128 + xt] = ex2(ell);
+          s_g[s * 128 + xt] = ex2(ell_ref - ell) * w;
           s_d[xt] = ex2(ltot - ell) * w;
         }
         if (xt == 0) s_elast[s] = ex2(ltot);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        if (rs == 0) {
+          float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int u = 0; u < TPT; ++u) {
-          const float d = s_dt[tb * TPT + u];
-          const float2 t01 = unpack_bf16x2(th_cur[u].x), t23 = unpack_bf16x2(th_cur[u].y);
-          acc[0] = fmaf(d, t01.x, acc[0]);
-          acc[1] = fmaf(d, t01.y, acc[1]);
-          acc[2] = fmaf(d, t23.x, acc[2]);
-          acc[3] = fmaf(d, t23.y, acc[3]);
+          for (int u = 0; u < TPT; ++u) {
+            const float d = s_dt[tb * TPT + u];
+            acc01 = __ffma2_rn(make_float2(d, d), unpack_bf16x2(th_cur[u].x), acc01);
+            acc23 = __ffma2_rn(make_float2(d, d), unpack_bf16x2(th_cur[u].y), acc23);
+          }
+          *reinterpret_cast<float4*>(&s_scan[tb * K + 4 * pg]) = make_float4(acc01.x, acc01.y, acc23.x, acc23.y);
         }
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq) s_scan[tb * K + 4 * pg + qq] = acc[qq];
       }
-      if (bar_sync_or(kBarXf, kRole, ab)) { ab = true; break; }
+      if (bar_sync_or(kBarXf, kXf, ab)) { ab = true; break; }
       // ---------------------------------------------------------- step C: rotate B, C; d X
       {
-        float ang[4];
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq) ang[qq] = s_carry[s * 64 + 4 * pg + qq];
-        for (int t2 = 0; t2 < tb; ++t2)
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq) ang[qq] += s_scan[t2 * K + 4 * pg + qq];
+        float4 base = *reinterpret_cast<const float4*>(&s_carry[s * 64 + 4 * pg]);
+        float a0 = base.x, a1 = base.y, a2v = base.z, a3 = base.w;
+        for (int t2 = 0; t2 < tb; ++t2) {
+          const float4 v = *reinterpret_cast<const float4*>(&s_scan[t2 * K + 4 * pg]);
+          a0 += v.x;
+          a1 += v.y;
+          a2v += v.z;
+          a3 += v.w;
+        }
         ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_FULL + s), (k >> 1) & 1, s_abort));
         if (!ab) {
           uint8_t* stg = sm + s * C::STAGE;
           const int nb = pg >> 3, c16 = pg & 7;
+          // Tokens in groups of up to four: angles and sin/cos of the whole group first,
+          // then the rows, so that independent work sits between dependent steps.
+          constexpr int UG = TPT < 4 ? TPT : 4;
 #pragma unroll
-          for (int u = 0; u < TPT; ++u) {
-            const float d = s_dt[tb * TPT + u];
-            const float2 t01 = unpack_bf16x2(th_cur[u].x), t23 = unpack_bf16x2(th_cur[u].y);
-            ang[0] = fmaf(d, t01.x, ang[0]);
-            ang[1] = fmaf(d, t01.y, ang[1]);
-            ang[2] = fmaf(d, t23.x, ang[2]);
-            ang[3] = fmaf(d, t23.y, ang[3]);
-            float cs[4], sn[4];
+          for (int u0 = 0; u0 < TPT; u0 += UG) {
+            float cs[UG][4], sn[UG][4];
 #pragma unroll
-            for (int qq = 0; qq < 4; ++qq) __sincosf(reduce_angle(ang[qq]), &sn[qq], &cs[qq]);
-            const int i = tb * TPT + u;
+            for (int uu = 0; uu < UG; ++uu) {
+              const float d = s_dt[tb * TPT + u0 + uu];
+              const float2 t01 = unpack_bf16x2(th_cur[u0 + uu].x), t23 = unpack_bf16x2(th_cur[u0 + uu].y);
+              a0 = fmaf(d, t01.x, a0);
+              a1 = fmaf(d, t01.y, a1);
+              a2v = fmaf(d, t23.x, a2v);
+              a3 = fmaf(d, t23.y, a3);
+              __sincosf(reduce_angle(a0), &sn[uu][0], &cs[uu][0]);
+              __sincosf(reduce_angle(a1), &sn[uu][1], &cs[uu][1]);
+              __sincosf(reduce_angle(a2v), &sn[uu][2], &cs[uu][2]);
+              __sincosf(reduce_angle(a3), &sn[uu][3], &cs[uu][3]);
+            }
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-              const uint32_t off = nb * 16384u + sw128(i * R + r, c16);
-              uint4 vb = *reinterpret_cast<const uint4*>(stg + off);
-              uint4 vc = *reinterpret_cast<const uint4*>(stg + C::TILE + off);
-              uint32_t* wb = reinterpret_cast<uint32_t*>(&vb);
-              uint32_t* wc = reinterpret_cast<uint32_t*>(&vc);
+            for (int uu = 0; uu < UG; ++uu) {
+              const int i = tb * TPT + u0 + uu;
 #pragma unroll
-              for (int qq = 0; qq < 4; ++qq) {
-                const float2 bb = unpack_bf16x2(wb[qq]), cc = unpack_bf16x2(wc[qq]);
-                const float b0 = cs[qq] * bb.x + sn[qq] * bb.y, b1 = -sn[qq] * bb.x + cs[qq] * bb.y;
-                const float c0 = cs[qq] * cc.x + sn[qq] * cc.y, c1 = -sn[qq] * cc.x + cs[qq] * cc.y;
-                range = fmaxf(range, fmaxf(fmaxf(fabsf(b0), fabsf(b1)), fmaxf(fabsf(c0), fabsf(c1))));
-                wb[qq] = pack_f16x2(b0, b1);
-                wc[qq] = pack_f16x2(c0, c1);
+              for (int r = rs; r < R; r += RS) {
+                const uint32_t off = nb * 16384u + sw128(i * R + r, c16);
+                uint4 vb = *reinterpret_cast<const uint4*>(stg + off);
+                uint4 vc = *reinterpret_cast<const uint4*>(stg + C::TILE + off);
+                uint32_t* wb = reinterpret_cast<uint32_t*>(&vb);
+                uint32_t* wc = reinterpret_cast<uint32_t*>(&vc);
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                  const float2 bb = unpack_bf16x2(wb[qq]), cc = unpack_bf16x2(wc[qq]);
+                  const float c = cs[uu][qq], sv = sn[uu][qq];
+                  // (u, v) -> (c u + s v, -s u + c v)
+                  const float b0 = fmaf(c, bb.x, sv * bb.y), b1 = fmaf(c, bb.y, -sv * bb.x);
+                  const float c0 = fmaf(c, cc.x, sv * cc.y), c1 = fmaf(c, cc.y, -sv * cc.x);
+                  range = fmaxf(range, fmaxf(fmaxf(fabsf(b0), fabsf(b1)), fmaxf(fabsf(c0), fabsf(c1))));
+                  wb[qq] = pack_f16x2(b0, b1);
+                  wc[qq] = pack_f16x2(c0, c1);
+                }
+                *reinterpret_cast<uint4*>(stg + off) = vb;
+                *reinterpret_cast<uint4*>(stg + C::TILE + off) = vc;
               }
-              *reinterpret_cast<uint4*>(stg + off) = vb;
-              *reinterpret_cast<uint4*>(stg + C::TILE + off) = vc;
             }
           }
-          if (tb == TB - 1) {
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) s_carry[(s ^ 1) * 64 + 4 * pg + qq] = reduce_angle(ang[qq]);
-          }
+          if (tb == TB - 1 && rs == 0)
+            *reinterpret_cast<float4*>(&s_carry[(s ^ 1) * 64 + 4 * pg]) =
+                make_float4(reduce_angle(a0), reduce_angle(a1), reduce_angle(a2v), reduce_angle(a3));
         }
         // d X into the single fp16 buffer, once GEMM4 of the previous chunk has read it
         if (k >= 1) ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_UFULL), (k - 1) & 1, s_abort));
+        ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_FULLX + s), (k >> 1) & 1, s_abort));
         if (!ab) {
           const uint8_t* sx = sm + s * C::STAGE + 2 * C::TILE;
           uint8_t* sdx = sm + C::OFF_DX;
-          const float dv = s_d[xt >> C::kLogR];
+          const int row = xt >> 1;
+          const float dv = s_d[row >> C::kLogR];
 #pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            const uint32_t off = sw128(xt, g);
+          for (int g = 0; g < 4; ++g) {
+            const uint32_t off = sw128(row, 4 * (xt & 1) + g);
             uint4 v = *reinterpret_cast<const uint4*>(sx + off);
             uint32_t* w = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq) {
               const float2 xx = unpack_bf16x2(w[qq]);
-              const float a0 = dv * xx.x, a1 = dv * xx.y;
-              range = fmaxf(range, fmaxf(fabsf(a0), fabsf(a1)));
-              w[qq] = pack_f16x2(a0, a1);
+              const float x0 = dv * xx.x, x1 = dv * xx.y;
+              range = fmaxf(range, fmaxf(fabsf(x0), fabsf(x1)));
+              w[qq] = pack_f16x2(x0, x1);
             }
             *reinterpret_cast<uint4*>(sdx + off) = v;
           }
@@ -489,53 +544,146 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           if (lane == 0) mbar_arrive(bar(B_XF + s));
         }
       }
-      cur_dt = nxt_dt;
-      cur_lam = nxt_lam;
-      qn_cur = qn_nxt;
+      dt_cur = dt_nxt;
+      lam_cur = lam_nxt;
+      qd_cur = qd_nxt;
+      ql_cur = ql_nxt;
 #pragma unroll
       for (int u = 0; u < TPT; ++u) th_cur[u] = th_nxt[u];
     }
     if (range > kF16Max) atomicOr(p.status, kDevRange);
     // ---------------------------------------------------------------- exit angle and token
-    bar_sync_or(kBarXf, kRole, ab);
+    bar_sync_or(kBarXf, kXf, ab);
     if (!ab) {
       if (p.phiT)
-        for (int k = xt; k < K; k += kRole)
+        for (int k = xt; k < K; k += kXf)
           p.phiT[static_cast<size_t>(bh) * K + k] = s_carry[(nchunks & 1) * 64 + k];
       const size_t last = (seq0 + static_cast<size_t>(T - 1) * tok_stride);
       if (p.prevBT)
-        for (int e = xt; e < R * NS; e += kRole)
+        for (int e = xt; e < R * NS; e += kXf)
           p.prevBT[static_cast<size_t>(bh) * R * NS + e] = p.B[last * R * NS + e];
       if (p.prevxT)
-        for (int e = xt; e < R * kP; e += kRole)
+        for (int e = xt; e < R * kP; e += kXf)
           p.prevxT[static_cast<size_t>(bh) * R * kP + e] = p.x[last * R * kP + e];
     }
-  } else {
-    // ================================================================ epilogue
-    const int q = warp & 3;          // TMEM lane quarter of this warp
-    const int ew = warp - kWarpEpi;  // epilogue warp index 0..3
-    const int i = q * 32 + lane;     // TMEM lane = chunk row = state row
+  } else if (warp < kWarpSy) {
+    // ================================================================ epilogue: mask
+    // One thread per TMEM lane = chunk row i; warp quarter q owns rows 32q..32q+31,
+    // whose tokens are exactly those of score column block q.
+    const int q = warp & 3;
+    const int i = q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    const bool srow = i < NS;
     const float* s_ell = misc + C::M_ELL;
     const float* s_w = misc + C::M_W;
     const float* s_gam = misc + C::M_GAM;
+    const float* s_g = misc + C::M_G;
+    const int ti = i >> C::kLogR;
+    for (int k = 0; k < nchunks; ++k) {
+      const int s = k & 1;
+      const uint32_t tS = tmem + TM_S + 128u * s;
+      // (the transform's arrival on B_XF publishes this chunk's decay sums and weights)
+      if (!__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_XF + s), (k >> 1) & 1, s_abort))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_SFULL + s), (k >> 1) & 1, s_abort))) break;
+      tc_fence_after();
+      const float* ell = s_ell + s * 128;
+      const float ell_i = ell[ti], gam_i = s_gam[s * 128 + ti];
+#pragma unroll 1
+      for (int blk = 0; blk < 4; ++blk) {
+        uint32_t hi[16], lo[16];
+        if (blk > q) {  // above the diagonal block: all zero
+#pragma unroll
+          for (int c = 0; c < 16; ++c) hi[c] = lo[c] = 0u;
+        } else if (blk < q) {  // strictly below: 2^{l_i - l_ref(blk)} * g_j
+          uint32_t sv[32];
+          tmem_ld32(tS + lane_off + 32u * blk, sv);
+          const float f = ex2(ell_i - ell[(blk + 1) * TPB - 1]);
+          const float* g = s_g + s * 128 + blk * TPB;
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float g0 = g[c >> C::kLogR], g1 = g[(c + 1) >> C::kLogR];
+            split2(make_float2(f * g0 * __uint_as_float(sv[c]), f * g1 * __uint_as_float(sv[c + 1])),
+                   hi[c >> 1], lo[c >> 1]);
+          }
+        } else {  // the diagonal block: direct decay
+          uint32_t sv[32];
+          tmem_ld32(tS + lane_off + 32u * blk, sv);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float m2[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int tj = (32 * blk + c + e) >> C::kLogR;
+              float m = 0.f;
+              if (tj < ti) m = ex2(ell_i - ell[tj]) * s_w[s * 128 + tj];
+              else if (tj == ti) m = gam_i;
+              m2[e] = m * __uint_as_float(sv[c + e]);
+            }
+            split2(make_float2(m2[0], m2[1]), hi[c >> 1], lo[c >> 1]);
+          }
+        }
+        tmem_st16(tS + lane_off + 32u * blk, hi);
+        tmem_st16(tS + lane_off + 32u * blk + 16u, lo);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(B_PFULL + s));
+        mbar_arrive(bar(B_MFREE + s));
+      }
+    }
+  } else {
+    // ================================================================ epilogue: state and y
+    const int q = warp & 3;        // TMEM lane quarter of this warp
+    const int ew = warp - kWarpSy; // warp index in the group, 0..3
+    const int i = q * 32 + lane;   // TMEM lane = chunk row = state row
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const bool swarp = q * 32 < NS;  // warp-uniform: this warp owns state rows
     const float* s_el = misc + C::M_EL;
     const float* s_elast = misc + C::M_ELAST;
     float* s_hmax = misc + C::M_HMAX;
     uint8_t* sHb = sm + C::OFF_H;
     const size_t seq0 = static_cast<size_t>(b) * T * H + head;
+    const uint32_t tH = tmem + TM_H + lane_off;
+    uint8_t* sYw = sm + C::OFF_Y + ew * 4096;  // this warp's y staging rows
+    const uint32_t sYs = sbase + C::OFF_Y + ew * 4096;
 
-    float hv[kP];
+    // fp16 copy of state row i (scaled by sig) as row i of the MN-major B operand of GEMM3
+    auto put_state_row = [&](float sig) {
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        uint32_t hv[32];
+        tmem_ld32(tH + 32u * half, hv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint4 w;
+          w.x = pack_f16x2(sig * __uint_as_float(hv[8 * g + 0]), sig * __uint_as_float(hv[8 * g + 1]));
+          w.y = pack_f16x2(sig * __uint_as_float(hv[8 * g + 2]), sig * __uint_as_float(hv[8 * g + 3]));
+          w.z = pack_f16x2(sig * __uint_as_float(hv[8 * g + 4]), sig * __uint_as_float(hv[8 * g + 5]));
+          w.w = pack_f16x2(sig * __uint_as_float(hv[8 * g + 6]), sig * __uint_as_float(hv[8 * g + 7]));
+          *reinterpret_cast<uint4*>(sHb + sw128(i, 4 * half + g)) = w;
+        }
+      }
+    };
+    auto warp_max = [&](float mx) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      return mx;
+    };
+
     // -------------------------------------------------------------- entry state
     // H' = h0 + q_0 B~_{-1} X_{-1}^T: the stored previous token rotated by its own angle
     // phi0, weighted by q_0 = (1 - lambda_0) dt_0 of this call's first token.
-    {
+    float mx0 = 0.f;
+    if (swarp) {
       const float q0 = (1.f - __bfloat162float(p.lam[seq0])) * __bfloat162float(p.dt[seq0]);
       float bt[R];
 #pragma unroll
       for (int r = 0; r < R; ++r) bt[r] = 0.f;
-      if (srow && p.prevB0) {
+      if (p.prevB0) {
         const int kk = i >> 1;
         const float ph = p.phi0 ? p.phi0[static_cast<size_t>(bh) * K + kk] : 0.f;
         float sn, cs;
@@ -547,11 +695,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           bt[r] = (i & 1) ? (-sn * u + cs * v) : (cs * u + sn * v);
         }
       }
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        uint32_t hv[32];
 #pragma unroll
-      for (int pp = 0; pp < kP; ++pp) {
-        float v = 0.f;
-        if (srow) {
-          if (p.h0) v = p.h0[(static_cast<size_t>(bh) * NS + i) * kP + pp];
+        for (int j = 0; j < 32; ++j) {
+          const int pp = 32 * half + j;
+          float v = p.h0 ? p.h0[(static_cast<size_t>(bh) * NS + i) * kP + pp] : 0.f;
           if (p.prevx0) {
             float f = 0.f;
 #pragma unroll
@@ -559,36 +709,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
               f = fmaf(bt[r], __bfloat162float(p.prevx0[(static_cast<size_t>(bh) * R + r) * kP + pp]), f);
             v = fmaf(q0, f, v);
           }
+          mx0 = fmaxf(mx0, fabsf(v));
+          hv[j] = __float_as_uint(v);
         }
-        hv[pp] = v;
+        tmem_st32(tH + 32u * half, hv);
       }
+      tmem_st_wait();
     }
-    // Scaled fp16 copy of the state as the K-major B operand of GEMM3 (row p, column n).
-    auto put_state = [&](float sig) {
-      if (srow) {
-        const uint32_t base = (i >> 6) * 8192u + (i & 7) * 2;
-#pragma unroll
-        for (int pp = 0; pp < kP; ++pp)
-          *reinterpret_cast<__half*>(sHb + base + sw128(pp, (i & 63) >> 3)) = __float2half_rn(sig * hv[pp]);
-      }
-    };
-    auto max_abs = [&]() {
-      float mx = 0.f;
-#pragma unroll
-      for (int pp = 0; pp < kP; ++pp) mx = fmaxf(mx, fabsf(hv[pp]));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      return mx;
-    };
     bool ab = false;
     float sig_cur;
     {
-      const float mx = max_abs();
-      if (lane == 0) s_hmax[ew] = mx;
-      bar_sync_or(kBarEpi, kRole, false);
+      mx0 = warp_max(mx0);
+      if (lane == 0) s_hmax[ew] = mx0;
+      bar_sync_or(kBarSy, kEpi, false);
       sig_cur = state_scale(fmaxf(fmaxf(s_hmax[0], s_hmax[1]), fmaxf(s_hmax[2], s_hmax[3])));
-      put_state(sig_cur);
+      if (swarp) put_state_row(sig_cur);
       fence_proxy_async_smem();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_STATE));
     }
@@ -596,115 +733,104 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     for (int k = 0; k < nchunks; ++k) {
       const int s = k & 1;
       const int t0 = k * CT;
-      const uint32_t tS = tmem + TM_S + 128u * s;
       const int ti = i >> C::kLogR;
-      // ---------------------------------------------------------- mask: S -> P (bf16 hi/lo)
-      // (the transform's arrival on B_XF publishes this chunk's decay sums and weights)
-      ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_XF + s), (k >> 1) & 1, s_abort));
-      ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_SFULL + s), (k >> 1) & 1, s_abort));
-      const float el_i = ab ? 0.f : s_el[s * 128 + ti];
-      if (!ab) {
-        tc_fence_after();
-        const float ell_i = s_ell[s * 128 + ti], gam_i = s_gam[s * 128 + ti];
-        const int whi = (q * 32 + 31) >> C::kLogR;  // last token among this warp's rows
-#pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
-          uint32_t hi[16], lo[16];
-          if (((32 * blk) >> C::kLogR) > whi) {
-#pragma unroll
-            for (int c = 0; c < 16; ++c) hi[c] = lo[c] = 0u;
-          } else {
-            uint32_t sv[32];
-            tmem_ld32(tS + lane_off + 32u * blk, sv);
-            tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              float m2[2];
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int tj = (32 * blk + c + e) >> C::kLogR;
-                float m = 0.f;
-                if (tj < ti) m = ex2(ell_i - s_ell[s * 128 + tj]) * s_w[s * 128 + tj];
-                else if (tj == ti) m = gam_i;
-                m2[e] = m * __uint_as_float(sv[c + e]);
-              }
-              split2(m2[0], m2[1], hi[c >> 1], lo[c >> 1]);
-            }
-          }
-          tmem_st16(tS + lane_off + 32u * blk, hi);
-          tmem_st16(tS + lane_off + 32u * blk + 16u, lo);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_PFULL + s));
-      }
       // ---------------------------------------------------------- state: H <- e^{L} H + U
+      ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_XF + s), (k >> 1) & 1, s_abort));
       ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_UFULL), k & 1, s_abort));
       ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_HFREE), k & 1, s_abort));
-      float mx = 0.f;
+      float mx = 0.f, el_i = 0.f;
       if (!ab) {
         tc_fence_after();
-        if (q * 32 < NS) {  // warp-uniform: this warp owns state rows
+        el_i = s_el[s * 128 + ti];
+        if (swarp) {
           const float eL = s_elast[s];
-#pragma unroll
+#pragma unroll 1
           for (int half = 0; half < 2; ++half) {
-            uint32_t uv[32];
+            uint32_t uv[32], hv[32];
             tmem_ld32(tmem + TM_U + lane_off + 32u * half, uv);
+            tmem_ld32(tH + 32u * half, hv);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) hv[32 * half + j] = fmaf(eL, hv[32 * half + j], __uint_as_float(uv[j]));
+            for (int j = 0; j < 32; ++j) {
+              const float h = fmaf(eL, __uint_as_float(hv[j]), __uint_as_float(uv[j]));
+              mx = fmaxf(mx, fabsf(h));
+              hv[j] = __float_as_uint(h);
+            }
+            tmem_st32(tH + 32u * half, hv);
           }
+          tmem_st_wait();
         }
-        mx = max_abs();
-        if (lane == 0) s_hmax[(s ^ 1) * 4 + ew] = mx;
+        mx = warp_max(mx);
+        if (lane == 0) {
+          s_hmax[(s ^ 1) * 4 + ew] = mx;
+          mbar_arrive(bar(B_MFREE + s));
+        }
       }
-      if (bar_sync_or(kBarEpi, kRole, ab)) { ab = true; break; }
+      if (bar_sync_or(kBarSy, kEpi, ab)) { ab = true; break; }
       const float sig_next = state_scale(fmaxf(fmaxf(s_hmax[(s ^ 1) * 4 + 0], s_hmax[(s ^ 1) * 4 + 1]),
                                                fmaxf(s_hmax[(s ^ 1) * 4 + 2], s_hmax[(s ^ 1) * 4 + 3])));
-      put_state(sig_next);
+      if (swarp) put_state_row(sig_next);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_STATE));
       // ---------------------------------------------------------- y = P X + e^{l} C~ H
+      // Each warp stages its 32 rows (128-byte swizzled) and one lane stores them with a
+      // TMA tensor store; rows past the end of the sequence are clipped by the store.
       ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_YFULL), k & 1, s_abort));
       if (!ab) {
         tc_fence_after();
         const float f = el_i / sig_cur;
-        const int r = i & (R - 1);
-        const int t = t0 + ti;
+        const int ty = t0 + (q * 32) / R;  // first token of this warp's rows
+        if (p.out_bf16) {
+          if (lane == 0) bulk_wait_group_read0();
+          __syncwarp();
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+            uint32_t a[32], c[32];
+            tmem_ld32(tmem + TM_YIN + lane_off + 32u * half, a);
+            tmem_ld32(tmem + TM_YOFF + lane_off + 32u * half, c);
+            tmem_ld_wait();
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t a[32], c[32];
-          tmem_ld32(tmem + TM_YIN + lane_off + 32u * half, a);
-          tmem_ld32(tmem + TM_YOFF + lane_off + 32u * half, c);
-          tmem_ld_wait();
-          if (t < T) {
-            const size_t o = ((seq0 + static_cast<size_t>(t) * H) * R + r) * kP + 32 * half;
-            if (p.out_bf16) {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) + o);
+            for (int g = 0; g < 4; ++g) {
+              uint32_t w[4];
 #pragma unroll
-              for (int qq = 0; qq < 4; ++qq) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int j = 8 * qq + 2 * e;
-                  w[e] = pack_bf16x2(fmaf(f, __uint_as_float(c[j]), __uint_as_float(a[j])),
-                                     fmaf(f, __uint_as_float(c[j + 1]), __uint_as_float(a[j + 1])));
-                }
-                dst[qq] = make_uint4(w[0], w[1], w[2], w[3]);
+              for (int e = 0; e < 4; ++e) {
+                const int j = 8 * g + 2 * e;
+                w[e] = pack_bf16x2(fmaf(f, __uint_as_float(c[j]), __uint_as_float(a[j])),
+                                   fmaf(f, __uint_as_float(c[j + 1]), __uint_as_float(a[j + 1])));
               }
-            } else {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.y) + o);
+              *reinterpret_cast<uint4*>(sYw + sw128(lane, 4 * half + g)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && ty < T) {  // a box wholly past the end stores nothing
+            tma_store_5d(&p.tmY, sYs, 0, 0, head, ty, b);
+            bulk_commit_group();
+          }
+        } else {
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+            uint32_t a[32], c[32];
+            tmem_ld32(tmem + TM_YIN + lane_off + 32u * half, a);
+            tmem_ld32(tmem + TM_YOFF + lane_off + 32u * half, c);
+            if (lane == 0) bulk_wait_group_read0();
+            __syncwarp();
+            tmem_ld_wait();
 #pragma unroll
-              for (int qq = 0; qq < 8; ++qq) {
-                float v[4];
+            for (int g = 0; g < 8; ++g) {
+              float v[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                  v[e] = fmaf(f, __uint_as_float(c[4 * qq + e]), __uint_as_float(a[4 * qq + e]));
-                dst[qq] = make_float4(v[0], v[1], v[2], v[3]);
-              }
+              for (int e = 0; e < 4; ++e)
+                v[e] = fmaf(f, __uint_as_float(c[4 * g + e]), __uint_as_float(a[4 * g + e]));
+              *reinterpret_cast<float4*>(sYw + sw128(lane, g)) = make_float4(v[0], v[1], v[2], v[3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && ty < T) {
+              tma_store_5d(&p.tmY, sYs, 32 * half, 0, head, ty, b);
+              bulk_commit_group();
             }
           }
         }
@@ -714,12 +840,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       }
       sig_cur = sig_next;
     }
+    if (lane == 0) bulk_wait_group0();  // every y store complete before the CTA exits
     // ---------------------------------------------------------------- exit state
-    if (!ab && p.hT && srow) {
+    if (!ab && p.hT && swarp) {
       float4* dst = reinterpret_cast<float4*>(p.hT + (static_cast<size_t>(bh) * NS + i) * kP);
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        uint32_t hv[32];
+        tmem_ld32(tH + 32u * half, hv);
+        tmem_ld_wait();
 #pragma unroll
-      for (int qq = 0; qq < kP / 4; ++qq)
-        dst[qq] = make_float4(hv[4 * qq], hv[4 * qq + 1], hv[4 * qq + 2], hv[4 * qq + 3]);
+        for (int qq = 0; qq < 8; ++qq)
+          dst[8 * half + qq] = make_float4(__uint_as_float(hv[4 * qq]), __uint_as_float(hv[4 * qq + 1]),
+                                           __uint_as_float(hv[4 * qq + 2]), __uint_as_float(hv[4 * qq + 3]));
+      }
     }
   }
 
@@ -744,19 +878,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 5-D map over [B][T][H][R][inner] bf16 with a box of {64, R, 1, ct, 1}.
-bool make_map(CUtensorMap* m, const void* ptr, int Bsz, int T, int H, int R, int inner, int ct) {
+// 5-D map over [B][T][H][R][inner] with a box of {box_inner, R, 1, ct, 1}, 128-byte swizzle
+// (box_inner elements make exactly 128 bytes).
+bool make_map(CUtensorMap* m, const void* ptr, int Bsz, int T, int H, int R, int inner, int ct,
+              CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t box_inner = 64u) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[5] = {(cuuint64_t)inner, (cuuint64_t)R, (cuuint64_t)H, (cuuint64_t)T,
                               (cuuint64_t)Bsz};
-  const cuuint64_t e = 2;
+  const cuuint64_t e = type == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? 4 : 2;
   const cuuint64_t strides[4] = {e * inner, e * inner * R, e * inner * R * H,
                                  e * inner * R * H * (cuuint64_t)T};
-  const cuuint32_t box[5] = {64u, (cuuint32_t)R, 1u, (cuuint32_t)ct, 1u};
+  const cuuint32_t box[5] = {box_inner, (cuuint32_t)R, 1u, (cuuint32_t)ct, 1u};
   const cuuint32_t es[5] = {1, 1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(ptr), dims, strides, box,
-                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = fn(m, type, 5, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -769,6 +905,11 @@ cudaError_t launch_nr(const PrefillArgs& a, cudaStream_t s) {
   if (!make_map(&p.tmB, a.B, d.B, d.T, d.H, R, NS, C::CT) ||
       !make_map(&p.tmC, a.C, d.B, d.T, d.H, R, NS, C::CT) ||
       !make_map(&p.tmX, a.x, d.B, d.T, d.H, R, kP, C::CT))
+    return cudaErrorInvalidValue;
+  const bool ybf = d.out_dtype == M3_BF16;
+  if (!make_map(&p.tmY, a.y, d.B, d.T, d.H, R, kP, 32 / R, ybf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                ybf ? 64u : 32u))
     return cudaErrorInvalidValue;
   p.x = static_cast<const __nv_bfloat16*>(a.x);
   p.B = static_cast<const __nv_bfloat16*>(a.B);
