@@ -292,7 +292,7 @@ def main():
     d = to_dev(inp, dev, torch)
     y = torch.empty(w.B, w.T, w.H, w.R, w.P, dtype=torch.float32, device=dev)
     hT = m3.State.zeros(w.B, w.H, w.N, w.P, w.R, device=dev)
-    ws = m3.workspace_for(m3.M3Dims(), dev)
+    ws = m3.prefill_workspace(d["x"], d["dt"], d["theta"])
 
     def prefill_step():
         m3.m3_ssm_prefill(d["x"], d["B"], d["C"], d["dt"], d["A"], d["lambda"], d["theta"], y=y,
@@ -364,9 +364,11 @@ def main():
         ym = torch.empty(wm.B, wm.T, wm.H, wm.R, wm.P, dtype=torch.float32, device=dev)
         hm = m3.State.zeros(wm.B, wm.H, wm.N, wm.P, wm.R, device=dev)
 
+        wsm = m3.prefill_workspace(dm["x"], dm["dt"], dm["theta"])
+
         def fm():
             m3.m3_ssm_prefill(dm["x"], dm["B"], dm["C"], dm["dt"], dm["A"], dm["lambda"],
-                              dm["theta"], y=ym, hT=hm, workspace=ws)
+                              dm["theta"], y=ym, hT=hm, workspace=wsm)
 
         for _ in range(3):
             fm()
@@ -389,9 +391,11 @@ def main():
                                            seed, wd.dtype), dev, torch)
             st = m3.State.zeros(wd.B, wd.H, wd.N, wd.P, wd.R, device=dev)
 
+            wsd = m3.prefill_workspace(pre["x"], pre["dt"], pre["theta"])
+
             def reset_state():
                 m3.m3_ssm_prefill(pre["x"], pre["B"], pre["C"], pre["dt"], pre["A"], pre["lambda"],
-                                  pre["theta"], hT=st, workspace=ws)
+                                  pre["theta"], hT=st, workspace=wsd)
 
             nsteps = args.decode_steps
             dsteps = []
@@ -436,9 +440,11 @@ def main():
         yl = torch.empty(wl.B, wl.T, wl.H, wl.R, wl.P, dtype=torch.float32, device=dev)
         sl = m3.State.zeros(wl.B, wl.H, wl.N, wl.P, wl.R, device=dev)
 
+        wsl = m3.prefill_workspace(dl["x"], dl["dt"], dl["theta"])
+
         def fl():
             m3.m3_ssm_prefill(dl["x"], dl["B"], dl["C"], dl["dt"], dl["A"], dl["lambda"],
-                              dl["theta"], y=yl, hT=sl, workspace=ws)
+                              dl["theta"], y=yl, hT=sl, workspace=wsl)
 
         for _ in range(3):
             fl()

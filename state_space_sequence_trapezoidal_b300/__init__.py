@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     m3_ssm_prefill,
     m3_ssm_prefill_noalloc,
     m3_ssm_prefill_workspace,
+    prefill_workspace,
     status_str,
     workspace_for,
 )

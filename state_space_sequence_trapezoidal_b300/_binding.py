@@ -147,9 +147,15 @@ def m3_ssm_prefill_workspace(dims: M3Dims) -> int:
 
 
 def workspace_for(dims: M3Dims, device) -> torch.Tensor:
-    """A zero-filled workspace tensor for m3_ssm_prefill."""
+    """A zero-filled workspace tensor for m3_ssm_prefill with these dimensions (the size
+    depends on the SM count of the current device)."""
     n = m3_ssm_prefill_workspace(dims)
     return torch.zeros((n + 15) // 16 * 16, dtype=torch.uint8, device=device)
+
+
+def prefill_workspace(x, dt, theta, out_dtype=torch.float32) -> torch.Tensor:
+    """A zero-filled workspace for m3_ssm_prefill on inputs shaped like these."""
+    return workspace_for(_dims(x, dt, theta, 0, x.dtype, out_dtype), x.device)
 
 
 def m3_ssm_prefill(x, B, C, dt, A, lam, theta, h0: State | None = None, *, y=None,

@@ -42,8 +42,10 @@ bool state_aligned(const m3_state* s) {
 extern "C" {
 
 size_t m3_ssm_prefill_workspace(const m3_dims* dims) {
-  (void)dims;
-  return kStatusBytes;
+  if (!dims || check_dims(dims, true) != M3_OK || !m3::prefill_tc_supported(*dims) || dims->T <= 0)
+    return kStatusBytes;
+  const size_t b = m3::tc_segments(*dims).bytes;
+  return b > kStatusBytes ? b : kStatusBytes;
 }
 
 const char* m3_status_str(m3_status s) {
@@ -95,6 +97,7 @@ m3_status m3_ssm_prefill(const m3_dims* dims, const void* x, const void* B, cons
   a.y = y;
   if (hT) a.hT = *hT;
   a.status = static_cast<unsigned*>(workspace);
+  a.ws = static_cast<uint8_t*>(workspace);
   if (!a.h0.h) a.h0 = m3_state{nullptr, nullptr, nullptr, nullptr};
   if (!a.hT.h) a.hT = m3_state{nullptr, nullptr, nullptr, nullptr};
 

@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda_runtime.h>
 #include <stddef.h>
+#include <stdint.h>
 
 #include "m3_ssm.h"
 
@@ -22,6 +23,7 @@ struct PrefillArgs {
   void* y;
   m3_state hT;  // all members null when no exit state is wanted
   unsigned* status;  // device status word (first bytes of the workspace)
+  uint8_t* ws;       // the workspace (status word first)
 };
 
 struct DecodeArgs {
@@ -39,6 +41,15 @@ struct DecodeArgs {
 
 // Tensor-core (tcgen05) chunked prefill: bf16 inputs, P = 64, N in {64, 128}, R in {1,2,4,8}.
 bool prefill_tc_supported(const m3_dims& d);
+
+// How the tensor-core prefill splits long sequences, and where the per-segment arrays sit
+// in the workspace (byte offsets; bytes = total workspace, status word included).
+struct TcSegments {
+  int nseg, seg_len;
+  size_t off_u, off_h, off_d, off_dphi, off_phi, bytes;
+};
+TcSegments tc_segments(const m3_dims& d);
+int sm_count();
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
 
 // CUDA-core recurrent prefill (fp32 arithmetic): every shape the API accepts.

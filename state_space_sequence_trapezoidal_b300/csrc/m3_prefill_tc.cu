@@ -111,6 +111,14 @@ struct TcParams {
   int out_bf16;
   int T, H;
   unsigned* status;
+  // Sequence segments (long sequences with few (batch row, head) pairs): segment s covers
+  // tokens [s * seg_len, (s + 1) * seg_len).  One segment = the whole sequence.
+  int seg_len, nseg;
+  float* wsU;        // [B*H][nseg-1][N][P]  zero-entry local-frame state at the end of segment s
+  float* wsD;        // [B*H][nseg-1]        decay over segment s
+  float* wsDphi;     // [B*H][nseg-1][N/2]   angle advanced over segment s
+  const float* wsH;  // [B*H][nseg-1][N][P]  entry state of segment s + 1 (trapezoid term folded in)
+  const float* wsPhi;  // [B*H][nseg-1][N/2] entry angle of segment s + 1
 };
 
 template <int NS, int R>
@@ -185,7 +193,10 @@ __device__ __forceinline__ float state_scale(float max_abs) {
   return __int_as_float(f << 23);
 }
 
-template <int NS, int R>
+// kStateOnly: the first pass over the segments of a long sequence.  Only B~ and the state
+// increments are formed (GEMM4), from a zero state at angle 0, and the segment's final
+// state, decay and angle advance go to the workspace; no output is written.
+template <int NS, int R, bool kStateOnly>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p) {
   using C = Cfg<NS, R>;
   constexpr int CT = C::CT, NB = C::NB, K = C::K, PG = C::PG, TB = C::TB, TPT = C::TPT;
@@ -202,9 +213,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.x, b = bh / p.H, head = bh % p.H, H = p.H;
-  const int T = p.T;
+  const int nsegx = kStateOnly ? p.nseg - 1 : p.nseg;
+  const int bh = blockIdx.x / nsegx, seg = blockIdx.x % nsegx;
+  const int b = bh / p.H, head = bh % p.H, H = p.H;
+  const int Tg = p.T;                        // tokens of the whole sequence
+  const int a0 = seg * p.seg_len;            // first token of this segment
+  const int T = min(p.seg_len, Tg - a0);     // tokens of this segment
   const int nchunks = (T + CT - 1) / CT;
+  const bool last_seg = !kStateOnly && seg == p.nseg - 1;
+  // entry state: the caller's for segment 0; for later segments the scanned one (its
+  // previous-token term already folded in); a zero state for the first pass
+  const size_t wi = static_cast<size_t>(bh) * (p.nseg - 1) + (seg - 1);
+  // (pointers to this sequence's own entry values)
+  const float* h0 = kStateOnly ? nullptr
+                  : seg > 0    ? p.wsH + wi * NS * kP
+                  : p.h0       ? p.h0 + static_cast<size_t>(bh) * NS * kP
+                               : nullptr;
+  const float* phi0 = kStateOnly ? nullptr
+                    : seg > 0    ? p.wsPhi + wi * K
+                    : p.phi0     ? p.phi0 + static_cast<size_t>(bh) * K
+                                 : nullptr;
+  const __nv_bfloat16* prevB0 =
+      (kStateOnly || seg > 0 || !p.prevB0) ? nullptr : p.prevB0 + static_cast<size_t>(bh) * R * NS;
+  const __nv_bfloat16* prevx0 =
+      (kStateOnly || seg > 0 || !p.prevx0) ? nullptr : p.prevx0 + static_cast<size_t>(bh) * R * kP;
   const float A2 = p.A[head] * kLog2e;
 
   if (tid == 0) {
@@ -242,17 +274,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const uint32_t st = sbase + s * C::STAGE;
         // B and C of chunk k once GEMM3 of chunk k - 2 has finished with this stage
         if (k >= 2 && !mbar_wait_abortable(bar(B_BCFREE + s), ((k >> 1) - 1) & 1, s_abort)) break;
-        mbar_arrive_expect_tx(bar(B_FULL + s), 2 * C::TILE);
+        mbar_arrive_expect_tx(bar(B_FULL + s), (kStateOnly ? 1 : 2) * C::TILE);
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
-          tma_load_5d(st + nb * 16384, &p.tmB, bar(B_FULL + s), 64 * nb, 0, head, k * CT, b);
-          tma_load_5d(st + C::TILE + nb * 16384, &p.tmC, bar(B_FULL + s), 64 * nb, 0, head, k * CT, b);
+          tma_load_5d(st + nb * 16384, &p.tmB, bar(B_FULL + s), 64 * nb, 0, head, a0 + k * CT, b);
+          if (!kStateOnly)
+            tma_load_5d(st + C::TILE + nb * 16384, &p.tmC, bar(B_FULL + s), 64 * nb, 0, head, a0 + k * CT, b);
         }
         issued[s] = k;
         // X of chunk k once GEMM2 of chunk k - 2 has finished with it
         if (k >= 2 && !mbar_wait_abortable(bar(B_XFREE + s), ((k >> 1) - 1) & 1, s_abort)) break;
         mbar_arrive_expect_tx(bar(B_FULLX + s), 16384);
-        tma_load_5d(st + 2 * C::TILE, &p.tmX, bar(B_FULLX + s), 0, 0, head, k * CT, b);
+        tma_load_5d(st + 2 * C::TILE, &p.tmX, bar(B_FULLX + s), 0, 0, head, a0 + k * CT, b);
         issuedx[s] = k;
       }
       // no copy may still be in flight when the CTA exits
@@ -271,7 +304,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       const uint32_t sDX = sbase + C::OFF_DX, sH = sbase + C::OFF_H;
       int last_bar = -1;
       uint32_t last_par = 0;
-      for (int k = 0; k < nchunks; ++k) {
+      if constexpr (kStateOnly) {
+        for (int k = 0; k < nchunks; ++k) {
+          const int s = k & 1;
+          const uint32_t sB = sbase + s * C::STAGE;
+          if (!mbar_wait_abortable(bar(B_XF + s), (k >> 1) & 1, s_abort)) break;
+          if (!mbar_wait_abortable(bar(B_STATE), k & 1, s_abort)) break;
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < kRows / 16; ++ks) {
+            const uint32_t kr = ks * 2048u;
+            tc_mma_ss(tmem + TM_U, sdesc_sw128(sB + kr, 16384, 1024), sdesc_sw128(sDX + kr, 16384, 1024),
+                      I_U, ks > 0);
+          }
+          tc_commit(bar(B_UFULL));
+          tc_commit(bar(B_BCFREE + s));
+          tc_commit(bar(B_XFREE + s));
+          last_bar = B_XFREE + s;
+          last_par = (k >> 1) & 1;
+        }
+      }
+      for (int k = 0; k < (kStateOnly ? 0 : nchunks); ++k) {
         const int s = k & 1;
         const uint32_t st = sbase + s * C::STAGE;
         const uint32_t sB = st, sC = st + C::TILE, sX = st + 2 * C::TILE;
@@ -351,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     float* s_carry = misc + C::M_CARRY;
     float* s_scan = misc + C::M_SCAN;
     const size_t tok_stride = static_cast<size_t>(H);
-    const size_t seq0 = static_cast<size_t>(b) * T * H + head;  // token 0 of this sequence
+    const size_t seq0 = (static_cast<size_t>(b) * Tg + a0) * H + head;  // token 0 of this segment
     const uint16_t* dt16 = reinterpret_cast<const uint16_t*>(p.dt);
     const uint16_t* lam16 = reinterpret_cast<const uint16_t*>(p.lam);
     auto bf = [](uint32_t bits16) { return __uint_as_float(bits16 << 16); };
@@ -367,8 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       d = dt16[o];
       l = lam16[o];
     };
-    auto load_q = [&](int kk, uint16_t& d, uint16_t& l) {  // chunk kk's first token
-      const size_t o = seq0 + static_cast<size_t>(clampT(kk * CT)) * tok_stride;
+    auto load_q = [&](int kk, uint16_t& d, uint16_t& l) {  // chunk kk's first token (may lie past the segment)
+      const int t = kk * CT < Tg - a0 ? kk * CT : Tg - a0 - 1;
+      const size_t o = seq0 + static_cast<size_t>(t) * tok_stride;
       d = dt16[o];
       l = lam16[o];
     };
@@ -388,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll
     for (int u = 0; u < TPT; ++u) th_nxt[u] = make_uint2(0u, 0u);
     for (int k = xt; k < K; k += kXf)
-      s_carry[k] = reduce_angle(p.phi0 ? p.phi0[static_cast<size_t>(bh) * K + k] : 0.f);
+      s_carry[k] = reduce_angle(phi0 ? phi0[k] : 0.f);
     float range = 0.f;  // largest |value| converted to fp16
     bool ab = false;
 
@@ -415,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         s_q[xt] = (1.f - cur_lam) * cur_dt;
         s_dt[xt] = cur_dt;
       }
-      if (xt == 0) s_q[CT] = (k + 1) * CT < T ? (1.f - bf(ql_cur)) * bf(qd_cur) : 0.f;
+      if (xt == 0) s_q[CT] = a0 + (k + 1) * CT < Tg ? (1.f - bf(ql_cur)) * bf(qd_cur) : 0.f;
       // both epilogue groups must be done with this misc slot (chunk k - 2)
       if (k >= 2)
         ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_MFREE + s), ((k >> 1) - 1) & 1, s_abort));
@@ -494,7 +548,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
               for (int r = rs; r < R; r += RS) {
                 const uint32_t off = nb * 16384u + sw128(i * R + r, c16);
                 uint4 vb = *reinterpret_cast<const uint4*>(stg + off);
-                uint4 vc = *reinterpret_cast<const uint4*>(stg + C::TILE + off);
+                uint4 vc = kStateOnly ? make_uint4(0u, 0u, 0u, 0u)
+                                      : *reinterpret_cast<const uint4*>(stg + C::TILE + off);
                 uint32_t* wb = reinterpret_cast<uint32_t*>(&vb);
                 uint32_t* wc = reinterpret_cast<uint32_t*>(&vc);
 #pragma unroll
@@ -509,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                   wc[qq] = pack_f16x2(c0, c1);
                 }
                 *reinterpret_cast<uint4*>(stg + off) = vb;
-                *reinterpret_cast<uint4*>(stg + C::TILE + off) = vc;
+                if (!kStateOnly) *reinterpret_cast<uint4*>(stg + C::TILE + off) = vc;
               }
             }
           }
@@ -554,7 +609,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     if (range > kF16Max) atomicOr(p.status, kDevRange);
     // ---------------------------------------------------------------- exit angle and token
     bar_sync_or(kBarXf, kXf, ab);
-    if (!ab) {
+    if (!ab && kStateOnly) {
+      for (int k = xt; k < K; k += kXf)
+        p.wsDphi[(static_cast<size_t>(bh) * (p.nseg - 1) + seg) * K + k] = s_carry[(nchunks & 1) * 64 + k];
+    }
+    if (!ab && last_seg) {
       if (p.phiT)
         for (int k = xt; k < K; k += kXf)
           p.phiT[static_cast<size_t>(bh) * K + k] = s_carry[(nchunks & 1) * 64 + k];
@@ -578,7 +637,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const float* s_gam = misc + C::M_GAM;
     const float* s_g = misc + C::M_G;
     const int ti = i >> C::kLogR;
-    for (int k = 0; k < nchunks; ++k) {
+    if constexpr (kStateOnly) {  // no scores: only release the decay sums of each chunk
+      for (int k = 0; k < nchunks; ++k) {
+        const int s = k & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_XF + s), (k >> 1) & 1, s_abort))) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_MFREE + s));
+      }
+    }
+    for (int k = 0; k < (kStateOnly ? 0 : nchunks); ++k) {
       const int s = k & 1;
       const uint32_t tS = tmem + TM_S + 128u * s;
       // (the transform's arrival on B_XF publishes this chunk's decay sums and weights)
@@ -645,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const float* s_elast = misc + C::M_ELAST;
     float* s_hmax = misc + C::M_HMAX;
     uint8_t* sHb = sm + C::OFF_H;
-    const size_t seq0 = static_cast<size_t>(b) * T * H + head;
+    const size_t seq0 = (static_cast<size_t>(b) * Tg + a0) * H + head;  // token 0 of this segment
     const uint32_t tH = tmem + TM_H + lane_off;
     uint8_t* sYw = sm + C::OFF_Y + ew * 4096;  // this warp's y staging rows
     const uint32_t sYs = sbase + C::OFF_Y + ew * 4096;
@@ -674,6 +741,68 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       return mx;
     };
 
+    if constexpr (kStateOnly) {
+      // zero state; per chunk H <- e^{L} H + U; the segment's H and decay to the workspace
+      bool ab = false;
+      float dprod = 1.f;
+      if (swarp) {
+        uint32_t z[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) z[j] = 0u;
+        tmem_st32(tH, z);
+        tmem_st32(tH + 32u, z);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_STATE));
+      for (int k = 0; k < nchunks && !ab; ++k) {
+        const int s = k & 1;
+        ab = !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_XF + s), (k >> 1) & 1, s_abort)) ||
+             !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_UFULL), k & 1, s_abort));
+        if (ab) break;
+        tc_fence_after();
+        const float eL = s_elast[s];
+        dprod *= eL;
+        if (swarp) {
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+            uint32_t uv[32], hv[32];
+            tmem_ld32(tmem + TM_U + lane_off + 32u * half, uv);
+            tmem_ld32(tH + 32u * half, hv);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              hv[j] = __float_as_uint(fmaf(eL, __uint_as_float(hv[j]), __uint_as_float(uv[j])));
+            tmem_st32(tH + 32u * half, hv);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(B_MFREE + s));
+          mbar_arrive(bar(B_STATE));
+        }
+      }
+      if (!ab) {
+        const size_t wo = static_cast<size_t>(bh) * (p.nseg - 1) + seg;
+        if (swarp) {
+          float4* dst = reinterpret_cast<float4*>(p.wsU + (wo * NS + i) * kP);
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+            uint32_t hv[32];
+            tmem_ld32(tH + 32u * half, hv);
+            tmem_ld_wait();
+#pragma unroll
+            for (int qq = 0; qq < 8; ++qq)
+              dst[8 * half + qq] = make_float4(__uint_as_float(hv[4 * qq]), __uint_as_float(hv[4 * qq + 1]),
+                                               __uint_as_float(hv[4 * qq + 2]), __uint_as_float(hv[4 * qq + 3]));
+          }
+        }
+        if (i == 0) p.wsD[wo] = dprod;
+      }
+    } else {
     // -------------------------------------------------------------- entry state
     // H' = h0 + q_0 B~_{-1} X_{-1}^T: the stored previous token rotated by its own angle
     // phi0, weighted by q_0 = (1 - lambda_0) dt_0 of this call's first token.
@@ -683,14 +812,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       float bt[R];
 #pragma unroll
       for (int r = 0; r < R; ++r) bt[r] = 0.f;
-      if (p.prevB0) {
+      if (prevB0) {
         const int kk = i >> 1;
-        const float ph = p.phi0 ? p.phi0[static_cast<size_t>(bh) * K + kk] : 0.f;
+        const float ph = phi0 ? phi0[kk] : 0.f;
         float sn, cs;
         sincosf(ph, &sn, &cs);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-          const __nv_bfloat16* pb = p.prevB0 + (static_cast<size_t>(bh) * R + r) * NS + 2 * kk;
+          const __nv_bfloat16* pb = prevB0 + r * NS + 2 * kk;
           const float u = __bfloat162float(pb[0]), v = __bfloat162float(pb[1]);
           bt[r] = (i & 1) ? (-sn * u + cs * v) : (cs * u + sn * v);
         }
@@ -701,12 +830,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int pp = 32 * half + j;
-          float v = p.h0 ? p.h0[(static_cast<size_t>(bh) * NS + i) * kP + pp] : 0.f;
-          if (p.prevx0) {
+          float v = h0 ? h0[i * kP + pp] : 0.f;
+          if (prevx0) {
             float f = 0.f;
 #pragma unroll
             for (int r = 0; r < R; ++r)
-              f = fmaf(bt[r], __bfloat162float(p.prevx0[(static_cast<size_t>(bh) * R + r) * kP + pp]), f);
+              f = fmaf(bt[r], __bfloat162float(prevx0[r * kP + pp]), f);
             v = fmaf(q0, f, v);
           }
           mx0 = fmaxf(mx0, fabsf(v));
@@ -781,7 +910,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       if (!ab) {
         tc_fence_after();
         const float f = el_i / sig_cur;
-        const int ty = t0 + (q * 32) / R;  // first token of this warp's rows
+        const int ty = a0 + t0 + (q * 32) / R;  // first token of this warp's rows
         if (p.out_bf16) {
           if (lane == 0) bulk_wait_group_read0();
           __syncwarp();
@@ -805,7 +934,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0 && ty < T) {  // a box wholly past the end stores nothing
+          if (lane == 0 && ty < Tg) {  // a box wholly past the end stores nothing
             tma_store_5d(&p.tmY, sYs, 0, 0, head, ty, b);
             bulk_commit_group();
           }
@@ -828,7 +957,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0 && ty < T) {
+            if (lane == 0 && ty < Tg) {
               tma_store_5d(&p.tmY, sYs, 32 * half, 0, head, ty, b);
               bulk_commit_group();
             }
@@ -842,7 +971,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     }
     if (lane == 0) bulk_wait_group0();  // every y store complete before the CTA exits
     // ---------------------------------------------------------------- exit state
-    if (!ab && p.hT && swarp) {
+    if (!ab && last_seg && p.hT && swarp) {
       float4* dst = reinterpret_cast<float4*>(p.hT + (static_cast<size_t>(bh) * NS + i) * kP);
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
@@ -855,6 +984,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                                            __uint_as_float(hv[4 * qq + 2]), __uint_as_float(hv[4 * qq + 3]));
       }
     }
+    }  // not state-only
   }
 
   tc_fence_before();
@@ -897,6 +1027,76 @@ bool make_map(CUtensorMap* m, const void* ptr, int Bsz, int T, int H, int R, int
   return r == CUDA_SUCCESS;
 }
 
+// Entry states of segments 1 .. nseg-1 of each sequence, from the first pass: a sequential
+// scan over the segments, H_in(s+1) = D_s H_in(s) + R(phi_in(s))^T U_s (the local-frame state
+// rotated pair by pair into the sequence's frame), phi_in(s+1) = phi_in(s) + dphi_s.
+// H_in(0) is the caller's entry state with the previous token's trapezoid term folded in.
+// One CTA per (batch row, head); thread = (state pair k, four head-dim columns).
+struct ScanParams {
+  int N, R, T, H, nseg;
+  const float* h0;
+  const float* phi0;
+  const __nv_bfloat16* prevB0;
+  const __nv_bfloat16* prevx0;
+  const __nv_bfloat16* dt;
+  const __nv_bfloat16* lam;
+  const float* wsU;
+  const float* wsD;
+  const float* wsDphi;
+  float* wsH;
+  float* wsPhi;
+};
+
+__global__ void __launch_bounds__(1024) segment_scan_kernel(const ScanParams p) {
+  const int bh = blockIdx.x, b = bh / p.H, head = bh % p.H;
+  const int N = p.N, K = N / 2, R = p.R;
+  const int k = threadIdx.x / (kP / 4), pc = (threadIdx.x % (kP / 4)) * 4;
+  if (k >= K) return;
+  const int n0 = 2 * k, n1 = 2 * k + 1;
+  float h[2][4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    h[0][c] = p.h0 ? p.h0[(static_cast<size_t>(bh) * N + n0) * kP + pc + c] : 0.f;
+    h[1][c] = p.h0 ? p.h0[(static_cast<size_t>(bh) * N + n1) * kP + pc + c] : 0.f;
+  }
+  float phi = p.phi0 ? p.phi0[static_cast<size_t>(bh) * K + k] : 0.f;
+  if (p.prevB0 && p.prevx0) {
+    const size_t t0 = static_cast<size_t>(b) * p.T * p.H + head;  // token 0
+    const float q0 = (1.f - __bfloat162float(p.lam[t0])) * __bfloat162float(p.dt[t0]);
+    float sn, cs;
+    sincosf(phi, &sn, &cs);
+    for (int r = 0; r < R; ++r) {
+      const float u = __bfloat162float(p.prevB0[(static_cast<size_t>(bh) * R + r) * N + n0]);
+      const float v = __bfloat162float(p.prevB0[(static_cast<size_t>(bh) * R + r) * N + n1]);
+      const float b0 = cs * u + sn * v, b1 = -sn * u + cs * v;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float x = __bfloat162float(p.prevx0[(static_cast<size_t>(bh) * R + r) * kP + pc + c]);
+        h[0][c] = fmaf(q0 * b0, x, h[0][c]);
+        h[1][c] = fmaf(q0 * b1, x, h[1][c]);
+      }
+    }
+  }
+  for (int sg = 0; sg + 1 < p.nseg; ++sg) {
+    const size_t wo = static_cast<size_t>(bh) * (p.nseg - 1) + sg;
+    const float D = p.wsD[wo];
+    float sn, cs;
+    sincosf(phi, &sn, &cs);
+    const float4 u0 = *reinterpret_cast<const float4*>(p.wsU + (wo * N + n0) * kP + pc);
+    const float4 u1 = *reinterpret_cast<const float4*>(p.wsU + (wo * N + n1) * kP + pc);
+    const float a0[4] = {u0.x, u0.y, u0.z, u0.w}, a1[4] = {u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      h[0][c] = fmaf(D, h[0][c], cs * a0[c] + sn * a1[c]);
+      h[1][c] = fmaf(D, h[1][c], -sn * a0[c] + cs * a1[c]);
+    }
+    *reinterpret_cast<float4*>(p.wsH + (wo * N + n0) * kP + pc) = make_float4(h[0][0], h[0][1], h[0][2], h[0][3]);
+    *reinterpret_cast<float4*>(p.wsH + (wo * N + n1) * kP + pc) = make_float4(h[1][0], h[1][1], h[1][2], h[1][3]);
+    phi = reduce_angle(phi + p.wsDphi[wo * K + k]);
+    if (pc == 0) p.wsPhi[wo * K + k] = phi;
+  }
+}
+
 template <int NS, int R>
 cudaError_t launch_nr(const PrefillArgs& a, cudaStream_t s) {
   using C = Cfg<NS, R>;
@@ -926,18 +1126,86 @@ cudaError_t launch_nr(const PrefillArgs& a, cudaStream_t s) {
   p.prevBT = static_cast<__nv_bfloat16*>(a.hT.prev_B);
   p.prevxT = static_cast<__nv_bfloat16*>(a.hT.prev_x);
   p.y = a.y;
-  p.out_bf16 = d.out_dtype == M3_BF16;
+  p.out_bf16 = ybf;
   p.T = d.T;
   p.H = d.H;
   p.status = a.status;
-  auto k = prefill_tc_kernel<NS, R>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_ALLOC);
+  const TcSegments sg = tc_segments(d);
+  p.seg_len = sg.seg_len;
+  p.nseg = sg.nseg;
+  p.wsU = reinterpret_cast<float*>(a.ws + sg.off_u);
+  p.wsH = reinterpret_cast<float*>(a.ws + sg.off_h);
+  p.wsD = reinterpret_cast<float*>(a.ws + sg.off_d);
+  p.wsDphi = reinterpret_cast<float*>(a.ws + sg.off_dphi);
+  p.wsPhi = reinterpret_cast<float*>(a.ws + sg.off_phi);
+  const unsigned bhn = static_cast<unsigned>(d.B) * static_cast<unsigned>(d.H);
+  cudaError_t e;
+  if (sg.nseg > 1) {
+    auto k1 = prefill_tc_kernel<NS, R, true>;
+    e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    k1<<<bhn * static_cast<unsigned>(sg.nseg - 1), kThreads, C::SMEM_ALLOC, s>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    ScanParams q{NS, R, d.T, d.H, sg.nseg, p.h0, p.phi0, p.prevB0, p.prevx0, p.dt, p.lam,
+                 p.wsU, p.wsD, p.wsDphi, p.wsU == nullptr ? nullptr : reinterpret_cast<float*>(a.ws + sg.off_h),
+                 reinterpret_cast<float*>(a.ws + sg.off_phi)};
+    segment_scan_kernel<<<bhn, (NS / 2) * (kP / 4), 0, s>>>(q);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  auto k = prefill_tc_kernel<NS, R, false>;
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
-  k<<<static_cast<unsigned>(d.B) * static_cast<unsigned>(d.H), kThreads, C::SMEM_ALLOC, s>>>(p);
+  k<<<bhn * static_cast<unsigned>(sg.nseg), kThreads, C::SMEM_ALLOC, s>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+int sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// Long sequences over few (batch row, head) pairs are split into segments so that about two
+// waves of CTAs fill the GPU; each segment is at least two chunks long.
+TcSegments tc_segments(const m3_dims& d) {
+  TcSegments g{};
+  g.nseg = 1;
+  g.seg_len = d.T;
+  const int ct = kRows / d.R;
+  const long long bhn = static_cast<long long>(d.B) * d.H;
+  const int sms = sm_count();
+  if (bhn > 0 && bhn < sms && d.T >= 4 * ct) {
+    const int chunks = (d.T + ct - 1) / ct;
+    long long want = (2LL * sms) / bhn;
+    if (want > chunks / 2) want = chunks / 2;
+    if (want >= 2) {
+      const int cps = static_cast<int>((chunks + want - 1) / want);
+      g.seg_len = cps * ct;
+      g.nseg = (d.T + g.seg_len - 1) / g.seg_len;
+    }
+  }
+  if (g.nseg > 1) {
+    const size_t m = static_cast<size_t>(bhn) * (g.nseg - 1);
+    auto up = [](size_t v) { return (v + 255) & ~size_t(255); };
+    g.off_u = 256;
+    g.off_h = g.off_u + up(m * d.N * kP * sizeof(float));
+    g.off_d = g.off_h + up(m * d.N * kP * sizeof(float));
+    g.off_dphi = g.off_d + up(m * sizeof(float));
+    g.off_phi = g.off_dphi + up(m * (d.N / 2) * sizeof(float));
+    g.bytes = g.off_phi + up(m * (d.N / 2) * sizeof(float));
+  } else {
+    g.bytes = 256;
+  }
+  return g;
+}
 
 bool prefill_tc_supported(const m3_dims& d) {
   return d.in_dtype == M3_BF16 && d.P == kP && (d.N == 64 || d.N == 128) &&

@@ -44,6 +44,20 @@ def random_state(B, H, N, P, R, dtype: str, seed: int) -> dict:
     return st
 
 
+def prior_state(B, H, N, P, R, dtype: str, seed: int, T0: int = 96) -> dict:
+    """An entry state of the kind a previous call hands over: the oracle's exit state after
+    T0 seeded tokens from rest (h, the unreduced angle, the raw last token).  Its magnitude
+    is that of the states the recurrence itself produces on these input distributions."""
+    inp = synth.make_inputs(B, T0, H, P, N, R, seed, dtype)
+    g = oracle.gather(inp, all_slices(B, H))
+    _, st, _ = oracle.scan(g["x"], g["Bm"], g["Cm"], g["dt"], g["A"], g["lam"], g["theta"])
+    out = {k: np.zeros((B, H) + v.shape[1:], np.float32) for k, v in st.items()}
+    for i, (b, h) in enumerate(all_slices(B, H)):
+        for k in st:
+            out[k][b, h] = st[k][i]
+    return out
+
+
 def state_to_device(st: dict, dtype: str, device="cuda") -> m3.State:
     return m3.State(torch.from_numpy(st["h"]).to(device),
                     torch.from_numpy(st["phi"]).to(device),

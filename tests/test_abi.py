@@ -83,6 +83,11 @@ def test_prefill_rejects_null_and_misaligned_pointers():
 
 def test_workspace_size():
     assert m3.m3_ssm_prefill_workspace(_dims()) >= 256
+    # a long sequence over few (batch row, head) pairs is split into segments, whose
+    # per-segment states live in the workspace
+    long = _dims(B=1, T=16384, H=32)
+    assert m3.m3_ssm_prefill_workspace(long) > 1 << 20
+    assert m3.m3_ssm_prefill_workspace(_dims(B=1, T=16384, H=32, in_dtype=0)) == 256
 
 
 def test_decode_rejects_bad_arguments():

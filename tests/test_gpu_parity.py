@@ -23,7 +23,7 @@ def prefill_gpu(inp_dev, h0=None, out_dtype=torch.float32, want_state=True, chun
     Bsz, T, H, R, Pd = x.shape
     N = inp_dev["B"].shape[-1]
     hT = m3.State.zeros(Bsz, H, N, Pd, R, dtype=x.dtype) if want_state else None
-    ws = m3.workspace_for(m3.M3Dims(Bsz, T, H, Pd, N, R, 0, 0, 0), x.device)
+    ws = m3.prefill_workspace(x, inp_dev["dt"], inp_dev["theta"], out_dtype)
     y = m3.m3_ssm_prefill(inp_dev["x"], inp_dev["B"], inp_dev["C"], inp_dev["dt"], inp_dev["A"],
                           inp_dev["lambda"], inp_dev["theta"], h0, hT=hT, workspace=ws,
                           out_dtype=out_dtype, chunk=chunk)
@@ -71,13 +71,52 @@ def test_bf16_tensor_core_prefill(N, R, fresh):
     CT = 128 // R
     T = 3 * CT + CT // 2 + 3
     inp = synth.make_inputs(B, T, H, Pd, N, R, 1000 + N + R, "bf16")
-    st0 = None if fresh else P.random_state(B, H, N, Pd, R, "bf16", 7)
+    st0 = None if fresh else P.prior_state(B, H, N, Pd, R, "bf16", 7)
     y, hT = prefill_gpu(P.to_device(inp, "bf16"),
                         None if fresh else P.state_to_device(st0, "bf16"))
     sl = P.all_slices(B, H)
     yr, sr = P.run_oracle(inp, sl, st0)
     e = P.rel_err(P.pick(y.cpu().numpy(), sl, True), yr)
     assert e <= P.TOL["bf16"], e
+    P.check_state({k: P.pick(v, sl, False) for k, v in P.state_to_host(hT).items()}, sr, "bf16")
+
+
+SEG_SHAPES = [(128, 1, 1500), (128, 2, 777), (64, 4, 600), (64, 8, 301)]
+
+
+@pytest.mark.parametrize("N,R,T", SEG_SHAPES)
+@pytest.mark.parametrize("fresh", [False, True])
+def test_segmented_long_sequence_prefill(N, R, T, fresh):
+    """Few (batch row, head) pairs and a long sequence: the sequence is split into segments
+    (first pass: per-segment local states; scan; second pass from the scanned entry states).
+    Every output and the exit state against the oracle, with and without an entry state."""
+    B, H, Pd = 1, 4, 64
+    inp = synth.make_inputs(B, T, H, Pd, N, R, 3000 + N + R + T, "bf16")
+    d = P.to_device(inp, "bf16")
+    assert m3.prefill_workspace(d["x"], d["dt"], d["theta"]).numel() > 256  # segmented
+    st0 = None if fresh else P.prior_state(B, H, N, Pd, R, "bf16", 17)
+    y, hT = prefill_gpu(d, None if fresh else P.state_to_device(st0, "bf16"))
+    sl = P.all_slices(B, H)
+    yr, sr = P.run_oracle(inp, sl, st0)
+    e = P.rel_err(P.pick(y.cpu().numpy(), sl, True), yr)
+    assert e <= P.TOL["bf16"], e
+    P.check_state({k: P.pick(v, sl, False) for k, v in P.state_to_host(hT).items()}, sr, "bf16")
+
+
+@pytest.mark.parametrize("N,R,T", [(128, 1, 1500), (64, 4, 600)])
+def test_oversized_entry_state(N, R, T):
+    """An entry state far larger than any state the recurrence produces (h ~ N(0, 1)): the
+    outputs it dominates are ~20x the sequence's RMS.  The tensor-core operands are fp16
+    (11 significant bits), so the error scales with each output's own magnitude; the bound
+    here is 2e-2 of the largest output, and the exit state still meets the RMS bound."""
+    B, H, Pd = 1, 4, 64
+    inp = synth.make_inputs(B, T, H, Pd, N, R, 4000 + N + R + T, "bf16")
+    st0 = P.random_state(B, H, N, Pd, R, "bf16", 19)
+    y, hT = prefill_gpu(P.to_device(inp, "bf16"), P.state_to_device(st0, "bf16"))
+    sl = P.all_slices(B, H)
+    yr, sr = P.run_oracle(inp, sl, st0)
+    got = P.pick(y.cpu().numpy(), sl, True)
+    assert np.max(np.abs(got - yr)) <= 2e-2 * np.max(np.abs(yr))
     P.check_state({k: P.pick(v, sl, False) for k, v in P.state_to_host(hT).items()}, sr, "bf16")
 
 
@@ -106,7 +145,7 @@ def test_continuation_across_calls(N, R, dtype):
     a = {k: (v[:, :T1].contiguous() if k != "A" else v) for k, v in dev.items()}
     b = {k: (v[:, T1:].contiguous() if k != "A" else v) for k, v in dev.items()}
     y1, st = prefill_gpu(a)
-    ws = m3.workspace_for(m3.M3Dims(), st.h.device)
+    ws = m3.prefill_workspace(b["x"], b["dt"], b["theta"])
     y2 = m3.m3_ssm_prefill(b["x"], b["B"], b["C"], b["dt"], b["A"], b["lambda"], b["theta"], st,
                            hT=st, workspace=ws)
     torch.cuda.synchronize()
