@@ -38,32 +38,64 @@ struct DecodeParams {
   int H, N, P;
 };
 
-// Threads: (P/4) column groups x RG row groups.  Thread (cg, rg) owns the
-// float4 columns 4cg..4cg+3 of rows rg, rg + RG, ..., rg + (VPT-1) RG.
-template <typename Tin, typename Tout, int R, int VPT>
-__global__ void __launch_bounds__(1024) decode_step_kernel(const DecodeParams p) {
+// R consecutive floats of one state row (rank-major factors stored [N][R]).
+template <int R>
+__device__ __forceinline__ void load_r(const float* src, float (&v)[R]) {
+  if constexpr (R % 4 == 0) {
+#pragma unroll
+    for (int q = 0; q < R / 4; ++q) {
+      const float4 t = reinterpret_cast<const float4*>(src)[q];
+      v[4 * q] = t.x;
+      v[4 * q + 1] = t.y;
+      v[4 * q + 2] = t.z;
+      v[4 * q + 3] = t.w;
+    }
+  } else if constexpr (R == 2) {
+    const float2 t = *reinterpret_cast<const float2*>(src);
+    v[0] = t.x;
+    v[1] = t.y;
+  } else {
+    v[0] = src[0];
+  }
+}
+
+// Threads: (P/2) column pairs x RG row groups.  Thread (cg, rg) owns columns
+// 2cg, 2cg+1 of rows rg, rg + RG, ..., rg + (VPT-1) RG.  The
+// rotated factors sit in shared memory rank-innermost ([N][R]) and the token's
+// X rows ([R][P]); each thread reads its own columns of X once and one short
+// vector of factors per state row, so the update runs from registers.
+// MAXT: 256 for the usual shapes, with enough CTAs per SM resident to keep the state
+// stream in flight (the register budget shrinks with that count); 1024 for states too
+// large to spread over 256 threads.
+template <int R, int MAXT>
+struct DecodeOcc {
+  static constexpr int kMinBlocks = MAXT > 256 ? 1 : (R <= 4 ? 4 : 2);
+};
+
+template <typename Tin, typename Tout, int R, int VPT, int MAXT>
+__global__ void __launch_bounds__(MAXT, DecodeOcc<R, MAXT>::kMinBlocks) decode_step_kernel(const DecodeParams p) {
   const int bh = blockIdx.x;
   const int head = bh % p.H;
   const int N = p.N, P = p.P, K = N >> 1;
-  const int P4 = P >> 2;
-  const int cg = threadIdx.x % P4;
-  const int rg = threadIdx.x / P4;
-  const int RG = blockDim.x / P4;
+  const int P2 = P >> 1;
+  const int cg = threadIdx.x % P2;  // column pair
+  const int rg = threadIdx.x / P2;
+  const int RG = blockDim.x / P2;
 
   float* hs = p.h + static_cast<size_t>(bh) * N * P;
-  float4 hv[VPT];
+  float2 hv[VPT];
 #pragma unroll
   for (int i = 0; i < VPT; ++i)
-    hv[i] = __ldcs(reinterpret_cast<const float4*>(hs + static_cast<size_t>(rg + i * RG) * P) + cg);
+    hv[i] = __ldcs(reinterpret_cast<const float2*>(hs + static_cast<size_t>(rg + i * RG) * P) + cg);
 
   extern __shared__ float sm[];
-  float* sBt = sm;               // [R][N] B~_t
-  float* sCt = sBt + R * N;      // [R][N] C~_t
-  float* sBp = sCt + R * N;      // [R][N] B~_{t-1}
+  float* sBt = sm;               // [N][R] B~_t
+  float* sCt = sBt + R * N;      // [N][R] C~_t
+  float* sBp = sCt + R * N;      // [N][R] B~_{t-1}
   float* sx = sBp + R * N;       // [R][P] X_t
   float* sxp = sx + R * P;       // [R][P] X_{t-1}
   float* red = sxp + R * P;      // [RG][R][P] partial outputs
-  float* sphi = red + RG * R * P;  // [K] advanced angle
+  float* sphi = red + RG * R * P; // [K] advanced angle
 
   const Tin* Bt = static_cast<const Tin*>(p.B);
   const Tin* Ct = static_cast<const Tin*>(p.C);
@@ -72,43 +104,56 @@ __global__ void __launch_bounds__(1024) decode_step_kernel(const DecodeParams p)
   const float lam = to_f(static_cast<const Tin*>(p.lam)[bh]);
   const Tin* th = static_cast<const Tin*>(p.theta) + static_cast<size_t>(bh) * K;
 
-  // Rotations: previous token by its own angle phi, current token by phi + dt theta.
-  // One thread per (rank column r, pair k), so the R columns rotate in parallel.
-  for (int i = threadIdx.x; i < R * K; i += blockDim.x) {
-    const int r = i / K, k = i - r * K;
-    const float ph0 = p.phi[static_cast<size_t>(bh) * K + k];
-    const float ph1 = ph0 + dt * to_f(th[k]);
+  // Prologue, one round of loads: thread i < R K rotates column r, pair k of the previous
+  // token (by its own angle phi) and of the current B and C (by phi + dt theta); thread
+  // i < R P copies the token's x.  The advanced angle is stored back reduced to [-pi, pi]
+  // so that long decode loops keep full precision.
+  const Tin* xt = static_cast<const Tin*>(p.x) + static_cast<size_t>(bh) * R * P;
+  Tin* prevx = static_cast<Tin*>(p.prevx) + static_cast<size_t>(bh) * R * P;
+  for (int i = threadIdx.x; i < R * K || i < R * P; i += blockDim.x) {
+    const bool rot = i < R * K, cpy = i < R * P;
+    const int r = rot ? i / K : 0, k = rot ? i - r * K : 0;
     const size_t o = (static_cast<size_t>(bh) * R + r) * N + 2 * k;
-    const float pu = to_f(prevB[o]), pv = to_f(prevB[o + 1]);
-    const Tin bu_raw = Bt[o], bv_raw = Bt[o + 1];
-    const float cu = to_f(Ct[o]), cv = to_f(Ct[o + 1]);
-    const float bu = to_f(bu_raw), bv = to_f(bv_raw);
-    float s0, c0, s1, c1;
-    sincosf(ph0, &s0, &c0);
-    sincosf(ph1, &s1, &c1);
-    sBp[r * N + 2 * k] = c0 * pu + s0 * pv;
-    sBp[r * N + 2 * k + 1] = -s0 * pu + c0 * pv;
-    sBt[r * N + 2 * k] = c1 * bu + s1 * bv;
-    sBt[r * N + 2 * k + 1] = -s1 * bu + c1 * bv;
-    sCt[r * N + 2 * k] = c1 * cu + s1 * cv;
-    sCt[r * N + 2 * k + 1] = -s1 * cu + c1 * cv;
-    prevB[o] = bu_raw;
-    prevB[o + 1] = bv_raw;
-    if (r == 0) sphi[k] = ph1;  // written back after the barrier: other columns read phi
-  }
-  {
-    const Tin* xt = static_cast<const Tin*>(p.x) + static_cast<size_t>(bh) * R * P;
-    Tin* prevx = static_cast<Tin*>(p.prevx) + static_cast<size_t>(bh) * R * P;
-    for (int i = threadIdx.x; i < R * P; i += blockDim.x) {
-      sxp[i] = to_f(prevx[i]);
-      const Tin v = xt[i];
-      sx[i] = to_f(v);
-      prevx[i] = v;
+    float ph0 = 0.f, thk = 0.f, pu = 0.f, pv = 0.f, cu = 0.f, cv = 0.f;
+    Tin bu_raw{}, bv_raw{}, xv{};
+    float xpv = 0.f;
+    if (rot) {
+      ph0 = p.phi[static_cast<size_t>(bh) * K + k];
+      thk = to_f(th[k]);
+      pu = to_f(prevB[o]);
+      pv = to_f(prevB[o + 1]);
+      bu_raw = Bt[o];
+      bv_raw = Bt[o + 1];
+      cu = to_f(Ct[o]);
+      cv = to_f(Ct[o + 1]);
+    }
+    if (cpy) {
+      xv = xt[i];
+      xpv = to_f(prevx[i]);
+    }
+    if (rot) {
+      const float ph1 = ph0 + dt * thk;
+      float s0, c0, s1, c1;
+      sincosf(ph0, &s0, &c0);
+      sincosf(ph1, &s1, &c1);
+      const float bu = to_f(bu_raw), bv = to_f(bv_raw);
+      sBp[(2 * k) * R + r] = c0 * pu + s0 * pv;
+      sBp[(2 * k + 1) * R + r] = -s0 * pu + c0 * pv;
+      sBt[(2 * k) * R + r] = c1 * bu + s1 * bv;
+      sBt[(2 * k + 1) * R + r] = -s1 * bu + c1 * bv;
+      sCt[(2 * k) * R + r] = c1 * cu + s1 * cv;
+      sCt[(2 * k + 1) * R + r] = -s1 * cu + c1 * cv;
+      prevB[o] = bu_raw;
+      prevB[o + 1] = bv_raw;
+      if (r == 0) sphi[k] = ph1;  // written back after the barrier: other columns read phi
+    }
+    if (cpy) {
+      sxp[i] = xpv;
+      sx[i] = to_f(xv);
+      prevx[i] = xv;
     }
   }
   __syncthreads();
-
-  // stored reduced to [-pi, pi] so that long decode loops keep full precision
   for (int k = threadIdx.x; k < K; k += blockDim.x)
     p.phi[static_cast<size_t>(bh) * K + k] =
         fmaf(-6.283185307179586f, rintf(sphi[k] * 0.15915494309189535f), sphi[k]);
@@ -117,35 +162,38 @@ __global__ void __launch_bounds__(1024) decode_step_kernel(const DecodeParams p)
   const float beta = (1.f - lam) * dt * alpha;
   const float gamma = lam * dt;
 
-  float yp[R][4];
+  // The thread's column pair goes through packed f32x2 FMAs: per rank, one FMA each for
+  // the previous-token and current-token products and one for the output.
+  float2 xr[R], xpr[R], yp[R];
 #pragma unroll
-  for (int r = 0; r < R; ++r) yp[r][0] = yp[r][1] = yp[r][2] = yp[r][3] = 0.f;
+  for (int r = 0; r < R; ++r) {
+    xr[r] = *reinterpret_cast<const float2*>(&sx[r * P + 2 * cg]);
+    xpr[r] = *reinterpret_cast<const float2*>(&sxp[r * P + 2 * cg]);
+    yp[r] = make_float2(0.f, 0.f);
+  }
+  const float2 a2 = make_float2(alpha, alpha);
 
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int n = rg + i * RG;
-    float hcur[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
+    float bp[R], bt[R], ct[R];
+    load_r<R>(&sBp[n * R], bp);
+    load_r<R>(&sBt[n * R], bt);
+    load_r<R>(&sCt[n * R], ct);
+    float2 prev = make_float2(0.f, 0.f), cur = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int pp = 4 * cg + j;
-      float prev = 0.f, cur = 0.f;
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        prev = fmaf(sBp[r * N + n], sxp[r * P + pp], prev);
-        cur = fmaf(sBt[r * N + n], sx[r * P + pp], cur);
-      }
-      hcur[j] = fmaf(alpha, hcur[j], fmaf(beta, prev, gamma * cur));
-#pragma unroll
-      for (int r = 0; r < R; ++r) yp[r][j] = fmaf(hcur[j], sCt[r * N + n], yp[r][j]);
+    for (int r = 0; r < R; ++r) {
+      prev = __ffma2_rn(make_float2(beta * bp[r], beta * bp[r]), xpr[r], prev);
+      cur = __ffma2_rn(make_float2(gamma * bt[r], gamma * bt[r]), xr[r], cur);
     }
-    __stcs(reinterpret_cast<float4*>(hs + static_cast<size_t>(n) * P) + cg,
-           make_float4(hcur[0], hcur[1], hcur[2], hcur[3]));
+    const float2 h = __ffma2_rn(a2, hv[i], __fadd2_rn(prev, cur));
+#pragma unroll
+    for (int r = 0; r < R; ++r) yp[r] = __ffma2_rn(h, make_float2(ct[r], ct[r]), yp[r]);
+    __stcs(reinterpret_cast<float2*>(hs + static_cast<size_t>(n) * P) + cg, h);
   }
 
 #pragma unroll
-  for (int r = 0; r < R; ++r)
-    *reinterpret_cast<float4*>(&red[(rg * R + r) * P + 4 * cg]) =
-        make_float4(yp[r][0], yp[r][1], yp[r][2], yp[r][3]);
+  for (int r = 0; r < R; ++r) *reinterpret_cast<float2*>(&red[(rg * R + r) * P + 2 * cg]) = yp[r];
   __syncthreads();
 
   Tout* y = static_cast<Tout*>(p.y) + static_cast<size_t>(bh) * R * P;
@@ -163,29 +211,33 @@ cudaError_t launch_r(const DecodeArgs& a, cudaStream_t s, int threads, int vpt) 
   const m3_dims& d = a.d;
   DecodeParams p{a.s.h, a.s.phi, a.s.prev_B, a.s.prev_x, a.x, a.B, a.C, a.dt, a.A, a.lam, a.theta,
                  a.y, d.H, d.N, d.P};
-  const int RG = threads / (d.P / 4);
+  const int RG = threads / (d.P / 2);
   const size_t smem = smem_bytes(d, RG);
   const dim3 grid(static_cast<unsigned>(d.B) * static_cast<unsigned>(d.H));
-  switch (vpt) {
-#define M3_CASE(V)                                                                             \
-  case V: {                                                                                    \
-    auto k = decode_step_kernel<Tin, Tout, R, V>;                                             \
-    if (smem > 48 * 1024) {                                                                    \
-      cudaError_t e =                                                                          \
-          cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);    \
-      if (e != cudaSuccess) return e;                                                          \
-    }                                                                                          \
-    k<<<grid, threads, smem, s>>>(p);                                                          \
-    return cudaGetLastError();                                                                 \
+  auto go = [&](auto k) -> cudaError_t {
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+    k<<<grid, threads, smem, s>>>(p);
+    return cudaGetLastError();
+  };
+  if (threads <= 256) {
+    switch (vpt) {
+      case 1: return go(decode_step_kernel<Tin, Tout, R, 1, 256>);
+      case 2: return go(decode_step_kernel<Tin, Tout, R, 2, 256>);
+      case 4: return go(decode_step_kernel<Tin, Tout, R, 4, 256>);
+      case 8: return go(decode_step_kernel<Tin, Tout, R, 8, 256>);
+      case 16: return go(decode_step_kernel<Tin, Tout, R, 16, 256>);
+      case 32: return go(decode_step_kernel<Tin, Tout, R, 32, 256>);
+      default: return cudaErrorInvalidValue;
+    }
   }
-    M3_CASE(1)
-    M3_CASE(2)
-    M3_CASE(4)
-    M3_CASE(8)
-    M3_CASE(16)
-#undef M3_CASE
-    default:
-      return cudaErrorInvalidValue;
+  switch (vpt) {
+    case 8: return go(decode_step_kernel<Tin, Tout, R, 8, 1024>);
+    case 16: return go(decode_step_kernel<Tin, Tout, R, 16, 1024>);
+    case 32: return go(decode_step_kernel<Tin, Tout, R, 32, 1024>);
+    default: return cudaErrorInvalidValue;
   }
 }
 
@@ -193,27 +245,27 @@ size_t smem_bytes(const m3_dims& d, int RG) {
   return sizeof(float) * (3 * d.R * d.N + 2 * d.R * d.P + RG * d.R * d.P + d.N / 2);
 }
 
-// Each thread keeps VPT in {1,2,4,8,16} float4 of state (VPT divides N), so
-// threads = (P/4) * (N / VPT).  Take the smallest VPT that gives at most 256
-// threads; failing that, the smallest that fits 1024 threads.
+// Each thread keeps VPT in {1,2,4,8,16,32} float2 of state (VPT divides N), so
+// threads = (P/2) * (N / VPT).  Take the smallest VPT that gives at most 256
+// threads; failing that, the smallest VPT >= 8 that fits 1024 threads.
 bool plan(const m3_dims& d, int* threads, int* vpt) {
   if (d.P % 4 != 0 || d.P < 4 || d.N < 2) return false;
-  const int P4 = d.P / 4;
+  const int P2 = d.P / 2;
   int fallback = 0;
-  for (int v = 1; v <= 16; v *= 2) {
+  for (int v = 1; v <= 32; v *= 2) {
     if (d.N % v != 0) continue;
-    const int t = P4 * (d.N / v);
+    const int t = P2 * (d.N / v);
     if (t > 1024 || smem_bytes(d, d.N / v) > 96 * 1024) continue;
     if (t <= 256) {
       *threads = t;
       *vpt = v;
       return true;
     }
-    if (fallback == 0) fallback = v;
+    if (fallback == 0 && v >= 8) fallback = v;
   }
   if (fallback == 0) return false;
   *vpt = fallback;
-  *threads = P4 * (d.N / fallback);
+  *threads = P2 * (d.N / fallback);
   return true;
 }
 
