@@ -148,12 +148,13 @@ struct Cfg {
   static constexpr int M_G = 1024;      // [2][128] 2^{l_ref - l_j} w_j
   static constexpr int M_ELAST = 1280;  // [2] 2^{l_last}
   static constexpr int M_D = 1284;      // [128] d_j
-  static constexpr int M_DT = 1412;     // [128] dt
-  static constexpr int M_Q = 1540;      // [129] q, then q of the next chunk's first token
-  static constexpr int M_WSUM = 1672;   // [8] warp totals of the log2-decay scan
-  static constexpr int M_HMAX = 1680;   // [2][4] per-warp max |h|
-  static constexpr int M_CARRY = 1688;  // [2][64] angle carried into a chunk
-  static constexpr int M_SCAN = 1816;   // [TB][K] angle partial sums
+  static constexpr int M_DT = 1412;     // [2][128] dt (read in step C while the next chunk's
+                                        //  step A may already write the other slot)
+  static constexpr int M_Q = 1668;      // [129] q, then q of the next chunk's first token
+  static constexpr int M_WSUM = 1800;   // [8] warp totals of the log2-decay scan
+  static constexpr int M_HMAX = 1808;   // [2][4] per-warp max |h|
+  static constexpr int M_CARRY = 1816;  // [2][64] angle carried into a chunk
+  static constexpr int M_SCAN = 1944;   // [TB][K] angle partial sums
   static constexpr int M_END = M_SCAN + TB * K;
   static constexpr uint32_t OFF_BAR = OFF_MISC + ((M_END * 4 + 15) / 16) * 16;
   static constexpr uint32_t OFF_HOLD = OFF_BAR + NUM_BARS * 8;  // TMEM base, abort flag
@@ -467,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       if (lane == 31) s_wsum[xw] = incl;
       if (xt < CT) {
         s_q[xt] = (1.f - cur_lam) * cur_dt;
-        s_dt[xt] = cur_dt;
+        s_dt[s * 128 + xt] = cur_dt;
       }
       if (xt == 0) s_q[CT] = a0 + (k + 1) * CT < Tg ? (1.f - bf(ql_cur)) * bf(qd_cur) : 0.f;
       // both epilogue groups must be done with this misc slot (chunk k - 2)
@@ -499,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
 #pragma unroll
           for (int u = 0; u < TPT; ++u) {
-            const float d = s_dt[tb * TPT + u];
+            const float d = s_dt[s * 128 + tb * TPT + u];
             acc01 = __ffma2_rn(make_float2(d, d), unpack_bf16x2(th_cur[u].x), acc01);
             acc23 = __ffma2_rn(make_float2(d, d), unpack_bf16x2(th_cur[u].y), acc23);
           }
@@ -530,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             float cs[UG][4], sn[UG][4];
 #pragma unroll
             for (int uu = 0; uu < UG; ++uu) {
-              const float d = s_dt[tb * TPT + u0 + uu];
+              const float d = s_dt[s * 128 + tb * TPT + u0 + uu];
               const float2 t01 = unpack_bf16x2(th_cur[u0 + uu].x), t23 = unpack_bf16x2(th_cur[u0 + uu].y);
               a0 = fmaf(d, t01.x, a0);
               a1 = fmaf(d, t01.y, a1);
