@@ -250,6 +250,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--skip-extras", action="store_true", help="headline prefill only")
+    ap.add_argument("--profile-decode", choices=["siso", "mimo"], default=None,
+                    help="run only --decode-steps plain decode steps of one decode workload "
+                         "(for profilers); prints their time, no bench line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -293,6 +296,26 @@ def main():
         clocks.mark(t0, time.time())
         D.barrier()
         return s.elapsed_time(e) / n
+
+    if args.profile_decode:
+        wd = synth.WORKLOADS[SISO_DEC if args.profile_decode == "siso" else MIMO_DEC]
+        inp = to_dev(synth.make_inputs(wd.B, 1, wd.H, wd.P, wd.N, wd.R, wd.seed, wd.dtype), dev,
+                     torch)
+        q = {k: (v[:, 0].contiguous() if k != "A" else v) for k, v in inp.items()}
+        st = m3.State.zeros(wd.B, wd.H, wd.N, wd.P, wd.R, device=dev)
+        st.h.normal_(0.0, 0.01)
+        yt = torch.empty(wd.B, wd.H, wd.R, wd.P, dtype=torch.float32, device=dev)
+
+        def one():
+            m3.m3_ssm_decode_step(st, q["x"], q["B"], q["C"], q["dt"], q["A"], q["lambda"],
+                                  q["theta"], y_t=yt)
+
+        for _ in range(args.warmup):
+            one()
+        ms = timed(one, args.decode_steps)
+        if rank == 0:
+            print(json.dumps({"profile_decode": wd.name, "us_per_step": ms * 1e3}), flush=True)
+        return 0
 
     # -------------------------------------------------------------- headline prefill
     w = synth.WORKLOADS[HEADLINE]
