@@ -314,7 +314,9 @@ def main():
             one()
         ms = timed(one, args.decode_steps)
         if rank == 0:
-            print(json.dumps({"profile_decode": wd.name, "us_per_step": ms * 1e3}), flush=True)
+            # plain launches from Python, for profiling only: not a bench figure
+            print(json.dumps({"profile_decode": wd.name, "us_per_step_host_launched": ms * 1e3}),
+                  flush=True)
         return 0
 
     # -------------------------------------------------------------- headline prefill
