@@ -72,6 +72,19 @@ def prefill_flops(w, rows=CHUNK_ROWS) -> int:
     return w.B * w.H * per_chunk * (-(-w.T // c_tok))
 
 
+def ssd_prefill_bytes(w, out_bytes=4) -> int:
+    """Mandatory HBM traffic of the Mamba-2 special case (no lambda, theta, angle or previous
+    token): x, B, C, dt in, y out, h_T."""
+    tok = w.B * w.T * w.H
+    return tok * (w.P * 2 + 2 * w.N * 2 + 2 + w.P * out_bytes) + w.B * w.H * w.N * w.P * 4 + w.H * 4
+
+
+def ssd_decode_bytes(w, out_bytes=4) -> int:
+    """One Mamba-2 decode step: state read + write, x, B, C, dt in, y out."""
+    bh = w.B * w.H
+    return bh * (2 * w.N * w.P * 4 + w.P * 2 + 2 * w.N * 2 + 2 + w.P * out_bytes) + w.H * 4
+
+
 def decode_bytes(w, out_bytes=4) -> int:
     """Mandatory HBM traffic of one decode step: state read + write, token inputs, y."""
     bh = w.B * w.H
@@ -466,6 +479,62 @@ def main():
             line["gpu_launches"] += nsteps
             del dsteps, pre, st
         line["decode"] = dec
+
+        # ---------------------------------------------------------- Mamba-2 special case
+        # The same shapes through m3_ssd_* (lambda = 1, theta = 0: no trapezoid term, no
+        # rotation, state h alone), as in the paper's Mamba-2 versus Mamba-3 decode table.
+        sx = {k: d[k][:, :, :, 0].contiguous() for k in ("x", "B", "C")}
+        ys = torch.empty(w.B, w.T, w.H, 1, w.P, dtype=torch.float32, device=dev)
+        hs = torch.zeros(w.B, w.H, w.N, w.P, dtype=torch.float32, device=dev)
+
+        def fs():
+            m3.m3_ssd_prefill(sx["x"], sx["B"], sx["C"], d["dt"], d["A"], None, y=ys, hT=hs,
+                              workspace=ws)
+
+        for _ in range(3):
+            fs()
+        mss = D.max_over_ranks(timed(fs, 20), dev)
+        bs = ssd_prefill_bytes(w)
+        wd = synth.WORKLOADS[SISO_DEC]
+        seed = D.rank_seed(wd.seed, rank)
+        nsteps = args.decode_steps
+        ssteps = []
+        for c0 in range(0, nsteps, 64):
+            seeds = [synth.decode_step_seed(seed, s) for s in range(c0, min(nsteps, c0 + 64))]
+            for si in gen_inputs_parallel(wd, seeds, A_seed=seed):
+                t = to_dev(si, dev, torch)
+                ssteps.append({k: (v[:, 0, :, 0].contiguous() if k in ("x", "B", "C") else
+                                   (v[:, 0].contiguous() if k == "dt" else v))
+                               for k, v in t.items() if k in ("x", "B", "C", "dt", "A")})
+        hsd = torch.zeros(wd.B, wd.H, wd.N, wd.P, dtype=torch.float32, device=dev)
+        ysd = torch.empty(wd.B, wd.H, 1, wd.P, dtype=torch.float32, device=dev)
+
+        def sloop():
+            for q in ssteps:
+                m3.m3_ssd_decode_step(hsd, q["x"], q["B"], q["C"], q["dt"], q["A"], y_t=ysd)
+
+        for q in ssteps[:3]:
+            m3.m3_ssd_decode_step(hsd, q["x"], q["B"], q["C"], q["dt"], q["A"], y_t=ysd)
+        torch.cuda.synchronize(dev)
+        sgraph = capture(sloop)
+        hsd.normal_(0.0, 0.05)
+        ms_sl = D.max_over_ranks(timed(sgraph.replay, 1), dev)
+        sper = ms_sl / nsteps
+        sdb = ssd_decode_bytes(wd)
+        m3_dec_us = dec[SISO_DEC]["us_per_step"]
+        line["mamba2"] = {
+            "prefill": {"workload": w.name, "ms": mss,
+                        "tokens_per_s": D.aggregate_throughput(w.B * w.T, world, mss / 1e3),
+                        "hbm_frac": bs / (mss / 1e3) / 1e9 / peaks["hbm_gbs"],
+                        "algorithmic_bytes": bs},
+            "decode": {"workload": wd.name, "steps": nsteps, "us_per_step": sper * 1e3,
+                       "tokens_per_s": D.aggregate_throughput(wd.B, world, sper / 1e3),
+                       "hbm_frac": sdb / (sper / 1e3) / 1e9 / peaks["hbm_gbs"],
+                       "algorithmic_bytes_per_step": sdb},
+            "mamba3_over_mamba2": {"prefill_time": ms_max / mss,
+                                   "decode_step_time": m3_dec_us / (sper * 1e3)}}
+        line["gpu_launches"] += 20 + nsteps
+        del sx, ys, hs, ssteps, hsd
 
         # ---------------------------------------------------------- 16384-token prefill + decode
         wl = synth.WORKLOADS[LONG]

@@ -176,6 +176,31 @@ m3_status m3_ssm_prefill_noalloc(const m3_dims* dims, const void* x, const void*
                                  const void* theta, const m3_state* h0, void* y,
                                  const m3_state* hT, void* stream);
 
+/*
+ * The Mamba-2 special case of the same layer core (paper section 2, Eq. (4), the
+ * exponential-Euler rule that Mamba-1 and Mamba-2 use, and Remark 5: the mask keeps
+ * only its diagonal weights), for the Mamba-2 versus Mamba-3 comparison of Table 6:
+ *
+ *   h_t = exp(dt_t A_h) h_{t-1} + dt_t B_t X_t^T,   y_t = h_t^T C_t
+ *
+ * i.e. the recurrence above with lambda = 1 (no trapezoid term) and theta = 0 (a real
+ * transition, no rotation).  SISO only (dims->R must be 1).  The state is h alone:
+ *   h0, hT, h   [B][H][N][P] float32 device pointers; h0 may be NULL (zero state), hT
+ *               may be NULL (not written) or equal h0 (in-place continuation).
+ * x, B, C, dt, A, y and their layouts, dtypes, alignment, workspace (sized by
+ * m3_ssm_prefill_workspace for the same dims), stream and status behaviour are those of
+ * m3_ssm_prefill / m3_ssm_decode_step.  The bf16 prefill with P = 64, N in {64, 128} runs
+ * on the tensor-core kernel with the rotation and the lambda terms compiled out; the
+ * decode step reads and writes the state exactly once.
+ */
+m3_status m3_ssd_prefill(const m3_dims* dims, const void* x, const void* B, const void* C,
+                         const void* dt, const float* A, const float* h0, void* y, float* hT,
+                         void* workspace, size_t ws_bytes, void* stream);
+
+m3_status m3_ssd_decode_step(const m3_dims* dims, float* h, const void* x_t, const void* B_t,
+                             const void* C_t, const void* dt_t, const float* A, void* y_t,
+                             void* stream);
+
 /* Short English description of a status code (static storage). */
 const char* m3_status_str(m3_status s);
 

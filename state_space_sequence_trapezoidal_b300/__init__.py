@@ -2,7 +2,8 @@
 
 The computation lives in ``libm3ssm.so`` (CUDA; C ABI in ``include/m3_ssm.h``):
 a chunked tcgen05/TMA prefill, a CUDA-core recurrent prefill for fp32, and a
-bandwidth-bound decode step.  This package is the thin Python binding.
+bandwidth-bound decode step, plus the Mamba-2 special case of both (lambda = 1,
+theta = 0) for the Mamba-2 versus Mamba-3 comparison.  This package is the thin Python binding.
 """
 from ._binding import (  # noqa: F401
     M3_BF16,
@@ -15,6 +16,8 @@ from ._binding import (  # noqa: F401
     State,
     library_path,
     load,
+    m3_ssd_decode_step,
+    m3_ssd_prefill,
     m3_ssm_decode_step,
     m3_ssm_device_status,
     m3_ssm_prefill,

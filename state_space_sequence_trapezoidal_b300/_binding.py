@@ -65,6 +65,10 @@ def load() -> ctypes.CDLL:
             lib.m3_ssm_prefill_noalloc.restype = ctypes.c_int
             lib.m3_ssm_decode_step.argtypes = [dp, sp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
             lib.m3_ssm_decode_step.restype = ctypes.c_int
+            lib.m3_ssd_prefill.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+            lib.m3_ssd_prefill.restype = ctypes.c_int
+            lib.m3_ssd_decode_step.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp]
+            lib.m3_ssd_decode_step.restype = ctypes.c_int
             lib.m3_ssm_device_status.argtypes = [vp, vp]
             lib.m3_ssm_device_status.restype = ctypes.c_int
             lib.m3_status_str.argtypes = [ctypes.c_int]
@@ -231,6 +235,69 @@ def m3_ssm_decode_step(state: State, x_t, B_t, C_t, dt_t, A, lam_t, theta_t, *, 
                                    _stream_handle(stream))
     if st != M3_OK:
         raise M3Error(st, "m3_ssm_decode_step")
+    return y_t
+
+
+def _ssd_dims(x, dt, N, prefill, in_dt, out_dt) -> M3Dims:
+    if prefill:
+        Bsz, T, H = dt.shape
+    else:
+        (Bsz, H), T = dt.shape, 0
+    return M3Dims(Bsz, T, H, x.shape[-1], N, 1, 0, _DT[in_dt], _DT[out_dt])
+
+
+def _check_state_h(h, d: M3Dims, dev, what):
+    if h is None:
+        return None
+    if (h.dtype != torch.float32 or not h.is_contiguous() or h.device != dev
+            or h.numel() != d.B * d.H * d.N * d.P):
+        raise ValueError(f"{what}: float32 [B,H,N,P] contiguous on {dev} expected")
+    return h.data_ptr()
+
+
+def m3_ssd_prefill(x, B, C, dt, A, h0=None, *, y=None, hT=None, workspace=None,
+                   out_dtype=torch.float32, stream=None):
+    """Mamba-2 special case (lambda = 1, theta = 0) of the prefill, SISO.  x [B,T,H,P],
+    B/C [B,T,H,N], dt [B,T,H], A [H] float32; h0 / hT optional float32 [B,H,N,P] states
+    (hT may be h0).  Returns y [B,T,H,1,P] in ``out_dtype``."""
+    in_dt = x.dtype
+    dev = _check_inputs(dict(x=x, B=B, C=C, dt=dt), in_dt)
+    _check_inputs(dict(A=A), torch.float32)
+    d = _ssd_dims(x, dt, B.shape[-1], True, in_dt, out_dtype)
+    if y is None:
+        y = torch.empty(d.B, d.T, d.H, 1, d.P, dtype=out_dtype, device=dev)
+    elif y.dtype != out_dtype or not y.is_contiguous() or y.numel() != d.B * d.T * d.H * d.P:
+        raise ValueError("y: wrong dtype, layout or size")
+    if workspace is None:
+        workspace = workspace_for(d, dev)
+    p0 = _check_state_h(h0, d, dev, "h0")
+    p1 = _check_state_h(hT, d, dev, "hT")
+    st = load().m3_ssd_prefill(ctypes.byref(d), x.data_ptr(), B.data_ptr(), C.data_ptr(),
+                               dt.data_ptr(), A.data_ptr(), p0, y.data_ptr(), p1,
+                               workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    if st != M3_OK:
+        raise M3Error(st, "m3_ssd_prefill")
+    return y
+
+
+def m3_ssd_decode_step(h, x_t, B_t, C_t, dt_t, A, *, y_t=None, out_dtype=torch.float32,
+                       stream=None):
+    """One Mamba-2 decode step, updating the float32 state ``h`` [B,H,N,P] in place.
+    x_t [B,H,P], B_t/C_t [B,H,N], dt_t [B,H].  Returns y_t [B,H,1,P] in ``out_dtype``."""
+    in_dt = x_t.dtype
+    dev = _check_inputs(dict(x_t=x_t, B_t=B_t, C_t=C_t, dt_t=dt_t), in_dt)
+    _check_inputs(dict(A=A), torch.float32)
+    d = _ssd_dims(x_t, dt_t, B_t.shape[-1], False, in_dt, out_dtype)
+    if y_t is None:
+        y_t = torch.empty(d.B, d.H, 1, d.P, dtype=out_dtype, device=dev)
+    ph = _check_state_h(h, d, dev, "h")
+    if ph is None:
+        raise ValueError("h: the state is required")
+    st = load().m3_ssd_decode_step(ctypes.byref(d), ph, x_t.data_ptr(), B_t.data_ptr(),
+                                   C_t.data_ptr(), dt_t.data_ptr(), A.data_ptr(), y_t.data_ptr(),
+                                   _stream_handle(stream))
+    if st != M3_OK:
+        raise M3Error(st, "m3_ssd_decode_step")
     return y_t
 
 

@@ -64,20 +64,28 @@ const char* m3_status_str(m3_status s) {
   return "unknown status";
 }
 
-m3_status m3_ssm_prefill(const m3_dims* dims, const void* x, const void* B, const void* C,
+}  // extern "C"
+
+namespace {
+
+// Shared by m3_ssm_prefill and m3_ssd_prefill; `ssd` selects the Mamba-2 special case
+// (lambda and theta null, state h only).
+m3_status prefill_common(const m3_dims* dims, const void* x, const void* B, const void* C,
                          const void* dt, const float* A, const void* lambda, const void* theta,
                          const m3_state* h0, void* y, const m3_state* hT, void* workspace,
-                         size_t ws_bytes, void* stream) {
+                         size_t ws_bytes, void* stream, bool ssd) {
   m3_status st = check_dims(dims, true);
   if (st != M3_OK) return st;
   const m3_dims& d = *dims;
-  if (h0 && !state_all_or_none(h0)) return M3_ERR_ARG;
-  if (hT && !state_all_or_none(hT)) return M3_ERR_ARG;
+  if (ssd && d.R != 1) return M3_ERR_SHAPE;
+  if (!ssd && h0 && !state_all_or_none(h0)) return M3_ERR_ARG;
+  if (!ssd && hT && !state_all_or_none(hT)) return M3_ERR_ARG;
   if (!workspace) return M3_ERR_WORKSPACE;
   if (ws_bytes < m3_ssm_prefill_workspace(dims)) return M3_ERR_WORKSPACE;
   const bool empty = d.B == 0 || d.H == 0;
   const bool has_tokens = !empty && d.T > 0;
-  if (has_tokens && (!x || !B || !C || !dt || !lambda || !theta || !y)) return M3_ERR_ARG;
+  if (has_tokens && (!x || !B || !C || !dt || !y)) return M3_ERR_ARG;
+  if (has_tokens && !ssd && (!lambda || !theta)) return M3_ERR_ARG;
   if (!empty && !A) return M3_ERR_ARG;
   if (!aligned16(x) || !aligned16(B) || !aligned16(C) || !aligned16(dt) || !aligned16(A) ||
       !aligned16(lambda) || !aligned16(theta) || !aligned16(y) || !aligned16(workspace))
@@ -114,6 +122,27 @@ m3_status m3_ssm_prefill(const m3_dims* dims, const void* x, const void* B, cons
   return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }
 
+}  // namespace
+
+extern "C" {
+
+m3_status m3_ssm_prefill(const m3_dims* dims, const void* x, const void* B, const void* C,
+                         const void* dt, const float* A, const void* lambda, const void* theta,
+                         const m3_state* h0, void* y, const m3_state* hT, void* workspace,
+                         size_t ws_bytes, void* stream) {
+  return prefill_common(dims, x, B, C, dt, A, lambda, theta, h0, y, hT, workspace, ws_bytes,
+                        stream, false);
+}
+
+m3_status m3_ssd_prefill(const m3_dims* dims, const void* x, const void* B, const void* C,
+                         const void* dt, const float* A, const float* h0, void* y, float* hT,
+                         void* workspace, size_t ws_bytes, void* stream) {
+  const m3_state s0{const_cast<float*>(h0), nullptr, nullptr, nullptr};
+  const m3_state s1{hT, nullptr, nullptr, nullptr};
+  return prefill_common(dims, x, B, C, dt, A, nullptr, nullptr, h0 ? &s0 : nullptr, y,
+                        hT ? &s1 : nullptr, workspace, ws_bytes, stream, true);
+}
+
 m3_status m3_ssm_decode_step(const m3_dims* dims, const m3_state* state, const void* x_t,
                              const void* B_t, const void* C_t, const void* dt_t, const float* A,
                              const void* lambda_t, const void* theta_t, void* y_t, void* stream) {
@@ -131,6 +160,24 @@ m3_status m3_ssm_decode_step(const m3_dims* dims, const m3_state* state, const v
       !aligned16(y_t))
     return M3_ERR_ALIGN;
   m3::DecodeArgs a{d, *state, x_t, B_t, C_t, dt_t, A, lambda_t, theta_t, y_t};
+  const cudaError_t e = m3::launch_decode(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+}
+
+m3_status m3_ssd_decode_step(const m3_dims* dims, float* h, const void* x_t, const void* B_t,
+                             const void* C_t, const void* dt_t, const float* A, void* y_t,
+                             void* stream) {
+  m3_status st = check_dims(dims, false);
+  if (st != M3_OK) return st;
+  const m3_dims& d = *dims;
+  if (d.R != 1 || !m3::decode_supported(d)) return M3_ERR_SHAPE;
+  if (d.B == 0 || d.H == 0) return M3_OK;
+  if (!h || !x_t || !B_t || !C_t || !dt_t || !A || !y_t) return M3_ERR_ARG;
+  if (!aligned16(h) || !aligned16(x_t) || !aligned16(B_t) || !aligned16(C_t) || !aligned16(dt_t) ||
+      !aligned16(A) || !aligned16(y_t))
+    return M3_ERR_ALIGN;
+  m3::DecodeArgs a{d, m3_state{h, nullptr, nullptr, nullptr}, x_t, B_t, C_t, dt_t, A, nullptr,
+                   nullptr, y_t};
   const cudaError_t e = m3::launch_decode(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }

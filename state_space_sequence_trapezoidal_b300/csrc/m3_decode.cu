@@ -72,7 +72,9 @@ struct DecodeOcc {
   static constexpr int kMinBlocks = MAXT > 256 ? 1 : (R <= 4 ? 4 : 2);
 };
 
-template <typename Tin, typename Tout, int R, int VPT, int MAXT>
+// kRot = false: the Mamba-2 special case (lambda = 1, theta = 0, Eq. (4)): h' = alpha h +
+// dt B_t X_t^T, y = h'^T C_t.  No angle, lambda or previous token is read or written.
+template <typename Tin, typename Tout, int R, int VPT, int MAXT, bool kRot>
 __global__ void __launch_bounds__(MAXT, DecodeOcc<R, MAXT>::kMinBlocks) decode_step_kernel(const DecodeParams p) {
   const int bh = blockIdx.x;
   const int head = bh % p.H;
@@ -101,16 +103,28 @@ __global__ void __launch_bounds__(MAXT, DecodeOcc<R, MAXT>::kMinBlocks) decode_s
   const Tin* Ct = static_cast<const Tin*>(p.C);
   Tin* prevB = static_cast<Tin*>(p.prevB);
   const float dt = to_f(static_cast<const Tin*>(p.dt)[bh]);
-  const float lam = to_f(static_cast<const Tin*>(p.lam)[bh]);
-  const Tin* th = static_cast<const Tin*>(p.theta) + static_cast<size_t>(bh) * K;
+  const float lam = kRot ? to_f(static_cast<const Tin*>(p.lam)[bh]) : 1.f;
+  const Tin* th = kRot ? static_cast<const Tin*>(p.theta) + static_cast<size_t>(bh) * K : nullptr;
 
   // Prologue, one round of loads: thread i < R K rotates column r, pair k of the previous
   // token (by its own angle phi) and of the current B and C (by phi + dt theta); thread
   // i < R P copies the token's x.  The advanced angle is stored back reduced to [-pi, pi]
   // so that long decode loops keep full precision.
   const Tin* xt = static_cast<const Tin*>(p.x) + static_cast<size_t>(bh) * R * P;
-  Tin* prevx = static_cast<Tin*>(p.prevx) + static_cast<size_t>(bh) * R * P;
-  for (int i = threadIdx.x; i < R * K || i < R * P; i += blockDim.x) {
+  Tin* prevx = kRot ? static_cast<Tin*>(p.prevx) + static_cast<size_t>(bh) * R * P : nullptr;
+  if constexpr (!kRot) {
+    for (int i = threadIdx.x; i < R * N || i < R * P; i += blockDim.x) {
+      if (i < R * N) {  // element n of column r, stored [N][R]
+        const int r = i / N, n = i - r * N;
+        const size_t o = (static_cast<size_t>(bh) * R + r) * N + n;
+        sBt[n * R + r] = to_f(Bt[o]);
+        sCt[n * R + r] = to_f(Ct[o]);
+      }
+      if (i < R * P) sx[i] = to_f(xt[i]);
+    }
+    __syncthreads();
+  }
+  for (int i = threadIdx.x; kRot && (i < R * K || i < R * P); i += blockDim.x) {
     const bool rot = i < R * K, cpy = i < R * P;
     const int r = rot ? i / K : 0, k = rot ? i - r * K : 0;
     const size_t o = (static_cast<size_t>(bh) * R + r) * N + 2 * k;
@@ -134,8 +148,8 @@ __global__ void __launch_bounds__(MAXT, DecodeOcc<R, MAXT>::kMinBlocks) decode_s
     if (rot) {
       const float ph1 = ph0 + dt * thk;
       float s0, c0, s1, c1;
-      sincosf(ph0, &s0, &c0);
-      sincosf(ph1, &s1, &c1);
+      __sincosf(fmaf(-6.283185307179586f, rintf(ph0 * 0.15915494309189535f), ph0), &s0, &c0);
+      __sincosf(fmaf(-6.283185307179586f, rintf(ph1 * 0.15915494309189535f), ph1), &s1, &c1);
       const float bu = to_f(bu_raw), bv = to_f(bv_raw);
       sBp[(2 * k) * R + r] = c0 * pu + s0 * pv;
       sBp[(2 * k + 1) * R + r] = -s0 * pu + c0 * pv;
@@ -153,8 +167,8 @@ __global__ void __launch_bounds__(MAXT, DecodeOcc<R, MAXT>::kMinBlocks) decode_s
       prevx[i] = xv;
     }
   }
-  __syncthreads();
-  for (int k = threadIdx.x; k < K; k += blockDim.x)
+  if constexpr (kRot) __syncthreads();
+  for (int k = threadIdx.x; kRot && k < K; k += blockDim.x)
     p.phi[static_cast<size_t>(bh) * K + k] =
         fmaf(-6.283185307179586f, rintf(sphi[k] * 0.15915494309189535f), sphi[k]);
 
@@ -168,7 +182,7 @@ __global__ void __launch_bounds__(MAXT, DecodeOcc<R, MAXT>::kMinBlocks) decode_s
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     xr[r] = *reinterpret_cast<const float2*>(&sx[r * P + 2 * cg]);
-    xpr[r] = *reinterpret_cast<const float2*>(&sxp[r * P + 2 * cg]);
+    xpr[r] = kRot ? *reinterpret_cast<const float2*>(&sxp[r * P + 2 * cg]) : make_float2(0.f, 0.f);
     yp[r] = make_float2(0.f, 0.f);
   }
   const float2 a2 = make_float2(alpha, alpha);
@@ -177,13 +191,13 @@ __global__ void __launch_bounds__(MAXT, DecodeOcc<R, MAXT>::kMinBlocks) decode_s
   for (int i = 0; i < VPT; ++i) {
     const int n = rg + i * RG;
     float bp[R], bt[R], ct[R];
-    load_r<R>(&sBp[n * R], bp);
+    if constexpr (kRot) load_r<R>(&sBp[n * R], bp);
     load_r<R>(&sBt[n * R], bt);
     load_r<R>(&sCt[n * R], ct);
     float2 prev = make_float2(0.f, 0.f), cur = make_float2(0.f, 0.f);
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      prev = __ffma2_rn(make_float2(beta * bp[r], beta * bp[r]), xpr[r], prev);
+      if constexpr (kRot) prev = __ffma2_rn(make_float2(beta * bp[r], beta * bp[r]), xpr[r], prev);
       cur = __ffma2_rn(make_float2(gamma * bt[r], gamma * bt[r]), xr[r], cur);
     }
     const float2 h = __ffma2_rn(a2, hv[i], __fadd2_rn(prev, cur));
@@ -206,7 +220,7 @@ __global__ void __launch_bounds__(MAXT, DecodeOcc<R, MAXT>::kMinBlocks) decode_s
 
 size_t smem_bytes(const m3_dims& d, int RG);
 
-template <typename Tin, typename Tout, int R>
+template <typename Tin, typename Tout, int R, bool kRot>
 cudaError_t launch_r(const DecodeArgs& a, cudaStream_t s, int threads, int vpt) {
   const m3_dims& d = a.d;
   DecodeParams p{a.s.h, a.s.phi, a.s.prev_B, a.s.prev_x, a.x, a.B, a.C, a.dt, a.A, a.lam, a.theta,
@@ -224,19 +238,19 @@ cudaError_t launch_r(const DecodeArgs& a, cudaStream_t s, int threads, int vpt) 
   };
   if (threads <= 256) {
     switch (vpt) {
-      case 1: return go(decode_step_kernel<Tin, Tout, R, 1, 256>);
-      case 2: return go(decode_step_kernel<Tin, Tout, R, 2, 256>);
-      case 4: return go(decode_step_kernel<Tin, Tout, R, 4, 256>);
-      case 8: return go(decode_step_kernel<Tin, Tout, R, 8, 256>);
-      case 16: return go(decode_step_kernel<Tin, Tout, R, 16, 256>);
-      case 32: return go(decode_step_kernel<Tin, Tout, R, 32, 256>);
+      case 1: return go(decode_step_kernel<Tin, Tout, R, 1, 256, kRot>);
+      case 2: return go(decode_step_kernel<Tin, Tout, R, 2, 256, kRot>);
+      case 4: return go(decode_step_kernel<Tin, Tout, R, 4, 256, kRot>);
+      case 8: return go(decode_step_kernel<Tin, Tout, R, 8, 256, kRot>);
+      case 16: return go(decode_step_kernel<Tin, Tout, R, 16, 256, kRot>);
+      case 32: return go(decode_step_kernel<Tin, Tout, R, 32, 256, kRot>);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (vpt) {
-    case 8: return go(decode_step_kernel<Tin, Tout, R, 8, 1024>);
-    case 16: return go(decode_step_kernel<Tin, Tout, R, 16, 1024>);
-    case 32: return go(decode_step_kernel<Tin, Tout, R, 32, 1024>);
+    case 8: return go(decode_step_kernel<Tin, Tout, R, 8, 1024, kRot>);
+    case 16: return go(decode_step_kernel<Tin, Tout, R, 16, 1024, kRot>);
+    case 32: return go(decode_step_kernel<Tin, Tout, R, 32, 1024, kRot>);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -280,12 +294,20 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   int threads, vpt;
   if (!plan(a.d, &threads, &vpt)) return cudaErrorInvalidValue;
   const bool bf_in = a.d.in_dtype == M3_BF16, bf_out = a.d.out_dtype == M3_BF16;
-#define M3_R(RR)                                                                                  \
-  if (a.d.R == RR) {                                                                              \
-    if (bf_in && bf_out) return launch_r<__nv_bfloat16, __nv_bfloat16, RR>(a, s, threads, vpt);  \
-    if (bf_in) return launch_r<__nv_bfloat16, float, RR>(a, s, threads, vpt);                    \
-    if (bf_out) return launch_r<float, __nv_bfloat16, RR>(a, s, threads, vpt);                   \
-    return launch_r<float, float, RR>(a, s, threads, vpt);                                        \
+  // No theta: the Mamba-2 special case, SISO only (state h alone).
+  if (!a.theta) {
+    if (a.d.R != 1 || a.lam || a.s.phi || a.s.prev_B || a.s.prev_x) return cudaErrorInvalidValue;
+    if (bf_in && bf_out) return launch_r<__nv_bfloat16, __nv_bfloat16, 1, false>(a, s, threads, vpt);
+    if (bf_in) return launch_r<__nv_bfloat16, float, 1, false>(a, s, threads, vpt);
+    if (bf_out) return launch_r<float, __nv_bfloat16, 1, false>(a, s, threads, vpt);
+    return launch_r<float, float, 1, false>(a, s, threads, vpt);
+  }
+#define M3_R(RR)                                                                                        \
+  if (a.d.R == RR) {                                                                                    \
+    if (bf_in && bf_out) return launch_r<__nv_bfloat16, __nv_bfloat16, RR, true>(a, s, threads, vpt);  \
+    if (bf_in) return launch_r<__nv_bfloat16, float, RR, true>(a, s, threads, vpt);                    \
+    if (bf_out) return launch_r<float, __nv_bfloat16, RR, true>(a, s, threads, vpt);                   \
+    return launch_r<float, float, RR, true>(a, s, threads, vpt);                                        \
   }
   M3_R(1)
   M3_R(2)

@@ -10,7 +10,8 @@
 // registers.  Per token: threads rotate B_t, C_t into shared memory (double
 // buffered, so the previous token's rotated B stays available for the beta
 // term), update their state entries, write partial outputs, and a fixed-order
-// reduction over g produces y_t.
+// reduction over g produces y_t.  With no lambda and no theta (null pointers) the
+// kernel runs the Mamba-2 special case, lambda = 1 and theta = 0.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -104,11 +105,11 @@ __global__ void __launch_bounds__(1024) prefill_recurrent_kernel(const RecParams
     const int cur = t & 1, prv = cur ^ 1;
     const size_t tok = (static_cast<size_t>(b) * T + t) * H + head;  // (b, t, head)
     const float dt = to_f(dtg[tok]);
-    const float lam = to_f(lamg[tok]);
+    const float lam = lamg ? to_f(lamg[tok]) : 1.f;  // no lambda, no theta: the Mamba-2 case
 
     // 1. advance the angle, rotate B_t and C_t; stage x_t.
     for (int k = threadIdx.x; k < K; k += blockDim.x) {
-      const float ph = sphi[k] + dt * to_f(thg[tok * K + k]);
+      const float ph = thg ? sphi[k] + dt * to_f(thg[tok * K + k]) : sphi[k];
       sphi[k] = fmaf(-6.283185307179586f, rintf(ph * 0.15915494309189535f), ph);  // keep |phi| <= pi
       float s, c;
       sincosf(ph, &s, &c);

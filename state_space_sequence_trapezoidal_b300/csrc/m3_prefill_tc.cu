@@ -197,7 +197,11 @@ __device__ __forceinline__ float state_scale(float max_abs) {
 // kStateOnly: the first pass over the segments of a long sequence.  Only B~ and the state
 // increments are formed (GEMM4), from a zero state at angle 0, and the segment's final
 // state, decay and angle advance go to the workspace; no output is written.
-template <int NS, int R, bool kStateOnly>
+// kRot = false: the Mamba-2 special case of the recurrence (lambda = 1, theta = 0: the
+// exponential-Euler rule of Eq. (4), real transition; Remark 5's diagonal-only mask).  No
+// lambda or theta is read, B and C are only converted to fp16, and the caller passes no
+// angle or previous token.
+template <int NS, int R, bool kStateOnly, bool kRot>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p) {
   using C = Cfg<NS, R>;
   constexpr int CT = C::CT, NB = C::NB, K = C::K, PG = C::PG, TB = C::TB, TPT = C::TPT;
@@ -416,22 +420,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     // zeroed at use (their dt is 0, which also cancels their theta).
     auto tok_of = [&](int kk) { return kk * CT + xt; };
     auto clampT = [&](int t) { return t < T ? t : T - 1; };
+    // Without the rotation (the Mamba-2 special case) lambda is 1 and theta 0: nothing of
+    // either is loaded (bf16 1.0 is 0x3f80).
     auto load_tok = [&](int kk, uint16_t& d, uint16_t& l) {
       const size_t o = seq0 + static_cast<size_t>(clampT(tok_of(kk))) * tok_stride;
       d = dt16[o];
-      l = lam16[o];
+      l = kRot ? lam16[o] : uint16_t(0x3f80);
     };
     auto load_q = [&](int kk, uint16_t& d, uint16_t& l) {  // chunk kk's first token (may lie past the segment)
       const int t = kk * CT < Tg - a0 ? kk * CT : Tg - a0 - 1;
       const size_t o = seq0 + static_cast<size_t>(t) * tok_stride;
       d = dt16[o];
-      l = lam16[o];
+      l = kRot ? lam16[o] : uint16_t(0x3f80);
     };
     auto load_th = [&](int kk, uint2 (&th)[TPT]) {
 #pragma unroll
       for (int u = 0; u < TPT; ++u) {
         const int t = clampT(kk * CT + tb * TPT + u);
-        th[u] = *reinterpret_cast<const uint2*>(p.theta + (seq0 + t * tok_stride) * K + 4 * pg);
+        th[u] = kRot ? *reinterpret_cast<const uint2*>(p.theta + (seq0 + t * tok_stride) * K + 4 * pg)
+                     : make_uint2(0u, 0u);
       }
     };
 
@@ -496,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           s_d[xt] = ex2(ltot - ell) * w;
         }
         if (xt == 0) s_elast[s] = ex2(ltot);
-        if (rs == 0) {
+        if (kRot && rs == 0) {
           float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
 #pragma unroll
           for (int u = 0; u < TPT; ++u) {
@@ -510,14 +517,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       if (bar_sync_or(kBarXf, kXf, ab)) { ab = true; break; }
       // ---------------------------------------------------------- step C: rotate B, C; d X
       {
-        float4 base = *reinterpret_cast<const float4*>(&s_carry[s * 64 + 4 * pg]);
-        float a0 = base.x, a1 = base.y, a2v = base.z, a3 = base.w;
-        for (int t2 = 0; t2 < tb; ++t2) {
-          const float4 v = *reinterpret_cast<const float4*>(&s_scan[t2 * K + 4 * pg]);
-          a0 += v.x;
-          a1 += v.y;
-          a2v += v.z;
-          a3 += v.w;
+        float a0 = 0.f, a1 = 0.f, a2v = 0.f, a3 = 0.f;
+        if constexpr (kRot) {
+          const float4 base = *reinterpret_cast<const float4*>(&s_carry[s * 64 + 4 * pg]);
+          a0 = base.x;
+          a1 = base.y;
+          a2v = base.z;
+          a3 = base.w;
+          for (int t2 = 0; t2 < tb; ++t2) {
+            const float4 v = *reinterpret_cast<const float4*>(&s_scan[t2 * K + 4 * pg]);
+            a0 += v.x;
+            a1 += v.y;
+            a2v += v.z;
+            a3 += v.w;
+          }
         }
         ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_FULL + s), (k >> 1) & 1, s_abort));
         if (!ab) {
@@ -531,6 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             float cs[UG][4], sn[UG][4];
 #pragma unroll
             for (int uu = 0; uu < UG; ++uu) {
+              if constexpr (!kRot) continue;
               const float d = s_dt[s * 128 + tb * TPT + u0 + uu];
               const float2 t01 = unpack_bf16x2(th_cur[u0 + uu].x), t23 = unpack_bf16x2(th_cur[u0 + uu].y);
               a0 = fmaf(d, t01.x, a0);
@@ -556,10 +570,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll
                 for (int qq = 0; qq < 4; ++qq) {
                   const float2 bb = unpack_bf16x2(wb[qq]), cc = unpack_bf16x2(wc[qq]);
-                  const float c = cs[uu][qq], sv = sn[uu][qq];
-                  // (u, v) -> (c u + s v, -s u + c v)
-                  const float b0 = fmaf(c, bb.x, sv * bb.y), b1 = fmaf(c, bb.y, -sv * bb.x);
-                  const float c0 = fmaf(c, cc.x, sv * cc.y), c1 = fmaf(c, cc.y, -sv * cc.x);
+                  float b0 = bb.x, b1 = bb.y, c0 = cc.x, c1 = cc.y;
+                  if constexpr (kRot) {
+                    const float c = cs[uu][qq], sv = sn[uu][qq];
+                    // (u, v) -> (c u + s v, -s u + c v)
+                    b0 = fmaf(c, bb.x, sv * bb.y);
+                    b1 = fmaf(c, bb.y, -sv * bb.x);
+                    c0 = fmaf(c, cc.x, sv * cc.y);
+                    c1 = fmaf(c, cc.y, -sv * cc.x);
+                  }
                   range = fmaxf(range, fmaxf(fmaxf(fabsf(b0), fabsf(b1)), fmaxf(fabsf(c0), fabsf(c1))));
                   wb[qq] = pack_f16x2(b0, b1);
                   wc[qq] = pack_f16x2(c0, c1);
@@ -569,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
               }
             }
           }
-          if (tb == TB - 1 && rs == 0)
+          if (kRot && tb == TB - 1 && rs == 0)
             *reinterpret_cast<float4*>(&s_carry[(s ^ 1) * 64 + 4 * pg]) =
                 make_float4(reduce_angle(a0), reduce_angle(a1), reduce_angle(a2v), reduce_angle(a3));
         }
@@ -612,7 +631,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     bar_sync_or(kBarXf, kXf, ab);
     if (!ab && kStateOnly) {
       for (int k = xt; k < K; k += kXf)
-        p.wsDphi[(static_cast<size_t>(bh) * (p.nseg - 1) + seg) * K + k] = s_carry[(nchunks & 1) * 64 + k];
+        p.wsDphi[(static_cast<size_t>(bh) * (p.nseg - 1) + seg) * K + k] =
+            kRot ? s_carry[(nchunks & 1) * 64 + k] : 0.f;
     }
     if (!ab && last_seg) {
       if (p.phiT)
@@ -809,7 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     // phi0, weighted by q_0 = (1 - lambda_0) dt_0 of this call's first token.
     float mx0 = 0.f;
     if (swarp) {
-      const float q0 = (1.f - __bfloat162float(p.lam[seq0])) * __bfloat162float(p.dt[seq0]);
+      const float q0 = kRot ? (1.f - __bfloat162float(p.lam[seq0])) * __bfloat162float(p.dt[seq0]) : 0.f;
       float bt[R];
 #pragma unroll
       for (int r = 0; r < R; ++r) bt[r] = 0.f;
@@ -1098,7 +1118,7 @@ __global__ void __launch_bounds__(1024) segment_scan_kernel(const ScanParams p) 
   }
 }
 
-template <int NS, int R>
+template <int NS, int R, bool kRot>
 cudaError_t launch_nr(const PrefillArgs& a, cudaStream_t s) {
   using C = Cfg<NS, R>;
   const m3_dims& d = a.d;
@@ -1142,7 +1162,7 @@ cudaError_t launch_nr(const PrefillArgs& a, cudaStream_t s) {
   const unsigned bhn = static_cast<unsigned>(d.B) * static_cast<unsigned>(d.H);
   cudaError_t e;
   if (sg.nseg > 1) {
-    auto k1 = prefill_tc_kernel<NS, R, true>;
+    auto k1 = prefill_tc_kernel<NS, R, true, kRot>;
     e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     k1<<<bhn * static_cast<unsigned>(sg.nseg - 1), kThreads, C::SMEM_ALLOC, s>>>(p);
@@ -1153,7 +1173,7 @@ cudaError_t launch_nr(const PrefillArgs& a, cudaStream_t s) {
     segment_scan_kernel<<<bhn, (NS / 2) * (kP / 4), 0, s>>>(q);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  auto k = prefill_tc_kernel<NS, R, false>;
+  auto k = prefill_tc_kernel<NS, R, false, kRot>;
   e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
   k<<<bhn * static_cast<unsigned>(sg.nseg), kThreads, C::SMEM_ALLOC, s>>>(p);
@@ -1214,8 +1234,15 @@ bool prefill_tc_supported(const m3_dims& d) {
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
+  // No theta: the Mamba-2 special case (lambda 1, no rotation, no previous token), SISO.
+  if (!a.theta) {
+    if (a.d.R != 1 || a.lam || a.h0.phi || a.h0.prev_B || a.h0.prev_x) return cudaErrorInvalidValue;
+    if (a.d.N == 128) return launch_nr<128, 1, false>(a, s);
+    if (a.d.N == 64) return launch_nr<64, 1, false>(a, s);
+    return cudaErrorInvalidValue;
+  }
 #define M3_NR(NN, RR) \
-  if (a.d.N == NN && a.d.R == RR) return launch_nr<NN, RR>(a, s);
+  if (a.d.N == NN && a.d.R == RR) return launch_nr<NN, RR, true>(a, s);
   M3_NR(128, 1)
   M3_NR(128, 2)
   M3_NR(128, 4)

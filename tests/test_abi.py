@@ -104,3 +104,29 @@ def test_decode_rejects_bad_arguments():
     assert call(_dims(), x=None) == ARG
     assert call(_dims(), x=40) == ALIGN
     assert call(_dims(), state=M3State(16, 16, None, 16)) == ARG
+
+
+def test_ssd_entry_points_reject_bad_arguments():
+    """The Mamba-2 special case: SISO only, lambda/theta absent, state h alone."""
+    lib = m3.load()
+
+    def pre(d, x=16, h0=None, hT=None, ws=16, wsb=256, y=16):
+        return lib.m3_ssd_prefill(ctypes.byref(d), x, 16, 16, 16, 16, h0, y, hT, ws, wsb, None)
+
+    def dec(d, h=16, x=16, y=16):
+        return lib.m3_ssd_decode_step(ctypes.byref(d), h, x, 16, 16, 16, 16, y, None)
+
+    assert pre(_dims(R=2)) == SHAPE
+    assert pre(_dims(N=7)) == SHAPE
+    assert pre(_dims(), x=None) == ARG
+    assert pre(_dims(), ws=None) == WS
+    assert pre(_dims(), wsb=8) == WS
+    assert pre(_dims(), y=8) == ALIGN
+    assert pre(_dims(), h0=24) == ALIGN
+    assert pre(_dims(), hT=40) == ALIGN
+    assert pre(_dims(chunk=64)) == UNSUP
+    assert dec(_dims(R=4)) == SHAPE
+    assert dec(_dims(), h=None) == ARG
+    assert dec(_dims(), x=None) == ARG
+    assert dec(_dims(), h=8) == ALIGN
+    assert dec(_dims(), y=4) == ALIGN
