@@ -18,6 +18,7 @@ draws its own inputs; a barrier and a max over ranks bracket the timed region.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -535,6 +536,32 @@ def main():
                                    "decode_step_time": m3_dec_us / (sper * 1e3)}}
         line["gpu_launches"] += 20 + nsteps
         del sx, ys, hs, ssteps, hsd
+
+        # ---------------------------------------------------------- backward of the prefill
+        # Gradients of every input for the headline shape (fp32 CUDA-core adjoint recurrence
+        # with checkpoints); dy in fp32 like y.
+        dyb = torch.randn(w.B, w.T, w.H, w.R, w.P, dtype=torch.float32, device=dev)
+        n_bws = m3.load().m3_ssm_prefill_backward_workspace(ctypes.byref(m3.M3Dims(
+            w.B, w.T, w.H, w.P, w.N, w.R, 0, m3.M3_BF16, m3.M3_F32)))
+        wsb = torch.empty((n_bws + 15) // 16 * 16, dtype=torch.uint8, device=dev)
+
+        def fb():
+            return m3.m3_ssm_prefill_backward(d["x"], d["B"], d["C"], d["dt"], d["A"], d["lambda"],
+                                              d["theta"], dyb, workspace=wsb)
+
+        fb()
+        msb = D.max_over_ranks(timed(fb, 3), dev)
+        tokh = w.B * w.T * w.H
+        bb = tokh * (w.R * w.P * 2 + 2 * w.R * w.N * 2 + 2 * 2 + (w.N // 2) * 2   # inputs
+                     + w.R * w.P * 4                                             # dy
+                     + (w.R * w.P + 2 * w.R * w.N + 2 + w.N // 2) * 4) + w.H * 8 # gradients
+        line["backward"] = {"workload": w.name, "ms": msb,
+                            "tokens_per_s": D.aggregate_throughput(w.B * w.T, world, msb / 1e3),
+                            "hbm_frac": bb / (msb / 1e3) / 1e9 / peaks["hbm_gbs"],
+                            "algorithmic_bytes": bb, "workspace_bytes": n_bws,
+                            "bound": "latency (one CTA per sequence, per-token barriers)"}
+        line["gpu_launches"] += 2 * 4
+        del dyb, wsb
 
         # ---------------------------------------------------------- 16384-token prefill + decode
         wl = synth.WORKLOADS[LONG]

@@ -201,6 +201,38 @@ m3_status m3_ssd_decode_step(const m3_dims* dims, float* h, const void* x_t, con
                              const void* C_t, const void* dt_t, const float* A, void* y_t,
                              void* stream);
 
+/*
+ * Backward pass of m3_ssm_prefill: the gradients a training step needs (paper section 1,
+ * "fast training kernels"; the masked form of section 2.3 / Eq. (7) is the same linear map
+ * as the recurrence, whose adjoint is run in reverse time).  For the loss
+ * L = <dy, y> + <dhT, h_T> of one prefill call with the given inputs and entry state:
+ *
+ *   dy     cotangent of y, [B][T][H][R][P] in dims->out_dtype (the dtype y had).
+ *   dhT    cotangent of the exit state h_T, float [B][H][N][P], or NULL (zero).
+ *   h0     the entry state the forward call used, or NULL (fresh sequence).
+ *   dx     float [B][T][H][R][P];   dB, dC float [B][T][H][R][N];
+ *   ddt, dlambda  float [B][T][H];  dtheta float [B][T][H][N/2];
+ *   dA     float [H], summed over batch rows and tokens (overwritten);
+ *   dh0    float [B][H][N][P], gradient with respect to the entry state's h, or NULL.
+ *          Gradients with respect to the entry state's angle and previous token are not
+ *          produced.
+ * All gradients are fp32 whatever the input dtype; the arithmetic is fp32 on CUDA cores
+ * (one CTA per (batch row, head): a forward pass that stores the state every few tokens in
+ * the workspace, then a reverse sweep that recomputes and walks back each stretch).
+ * Supported when N * P <= 8192 (so that each thread holds at most 8 state rows of one
+ * column); other shapes return M3_ERR_SHAPE.  Inputs, dtypes, alignment and stream
+ * behaviour as m3_ssm_prefill; the workspace must hold m3_ssm_prefill_backward_workspace
+ * bytes (its contents need no initialisation).  dims->chunk is ignored.
+ */
+size_t m3_ssm_prefill_backward_workspace(const m3_dims* dims);
+
+m3_status m3_ssm_prefill_backward(const m3_dims* dims, const void* x, const void* B, const void* C,
+                                  const void* dt, const float* A, const void* lambda,
+                                  const void* theta, const m3_state* h0, const void* dy,
+                                  const float* dhT, float* dx, float* dB, float* dC, float* ddt,
+                                  float* dA, float* dlambda, float* dtheta, float* dh0,
+                                  void* workspace, size_t ws_bytes, void* stream);
+
 /* Short English description of a status code (static storage). */
 const char* m3_status_str(m3_status s);
 

@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     m3_ssm_decode_step,
     m3_ssm_device_status,
     m3_ssm_prefill,
+    m3_ssm_prefill_backward,
     m3_ssm_prefill_noalloc,
     m3_ssm_prefill_workspace,
     prefill_workspace,

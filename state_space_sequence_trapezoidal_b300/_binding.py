@@ -65,6 +65,10 @@ def load() -> ctypes.CDLL:
             lib.m3_ssm_prefill_noalloc.restype = ctypes.c_int
             lib.m3_ssm_decode_step.argtypes = [dp, sp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
             lib.m3_ssm_decode_step.restype = ctypes.c_int
+            lib.m3_ssm_prefill_backward_workspace.argtypes = [dp]
+            lib.m3_ssm_prefill_backward_workspace.restype = sz
+            lib.m3_ssm_prefill_backward.argtypes = [dp] + [vp] * 7 + [sp] + [vp] * 10 + [vp, sz, vp]
+            lib.m3_ssm_prefill_backward.restype = ctypes.c_int
             lib.m3_ssd_prefill.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
             lib.m3_ssd_prefill.restype = ctypes.c_int
             lib.m3_ssd_decode_step.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp]
@@ -299,6 +303,48 @@ def m3_ssd_decode_step(h, x_t, B_t, C_t, dt_t, A, *, y_t=None, out_dtype=torch.f
     if st != M3_OK:
         raise M3Error(st, "m3_ssd_decode_step")
     return y_t
+
+
+def m3_ssm_prefill_backward(x, B, C, dt, A, lam, theta, dy, h0: State | None = None, *,
+                            dhT=None, want_dh0=False, workspace=None, stream=None) -> dict:
+    """Gradients of L = <dy, y> + <dhT, h_T> for the prefill with these inputs (shapes as
+    ``m3_ssm_prefill``; dy like y, in the dtype y had; dhT float32 [B,H,N,P] or None).
+    Returns float32 tensors dx, dB, dC, ddt, dA [H], dlambda, dtheta and, if ``want_dh0``,
+    dh0 [B,H,N,P]."""
+    in_dt = x.dtype
+    dev = _check_inputs(dict(x=x, B=B, C=C, dt=dt, lam=lam, theta=theta), in_dt)
+    _check_inputs(dict(A=A), torch.float32)
+    d = _dims(x, dt, theta, 0, in_dt, dy.dtype)
+    _check_inputs(dict(dy=dy), dy.dtype)
+    if dy.numel() != d.B * d.T * d.H * d.R * d.P:
+        raise ValueError("dy: wrong size")
+    if dhT is not None and (dhT.dtype != torch.float32 or not dhT.is_contiguous()
+                            or dhT.numel() != d.B * d.H * d.N * d.P):
+        raise ValueError("dhT: float32 [B,H,N,P] contiguous expected")
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = {"dx": torch.empty(d.B, d.T, d.H, d.R, d.P, **f32),
+         "dB": torch.empty(d.B, d.T, d.H, d.R, d.N, **f32),
+         "dC": torch.empty(d.B, d.T, d.H, d.R, d.N, **f32),
+         "ddt": torch.empty(d.B, d.T, d.H, **f32), "dA": torch.empty(d.H, **f32),
+         "dlambda": torch.empty(d.B, d.T, d.H, **f32),
+         "dtheta": torch.empty(d.B, d.T, d.H, d.N // 2, **f32)}
+    if want_dh0:
+        g["dh0"] = torch.empty(d.B, d.H, d.N, d.P, **f32)
+    if workspace is None:
+        n = int(load().m3_ssm_prefill_backward_workspace(ctypes.byref(d)))
+        workspace = torch.empty((n + 15) // 16 * 16, dtype=torch.uint8, device=dev)
+    c0 = h0._c() if h0 is not None else None
+    st = load().m3_ssm_prefill_backward(
+        ctypes.byref(d), x.data_ptr(), B.data_ptr(), C.data_ptr(), dt.data_ptr(), A.data_ptr(),
+        lam.data_ptr(), theta.data_ptr(), ctypes.byref(c0) if c0 is not None else None,
+        dy.data_ptr(), dhT.data_ptr() if dhT is not None else None, g["dx"].data_ptr(),
+        g["dB"].data_ptr(), g["dC"].data_ptr(), g["ddt"].data_ptr(), g["dA"].data_ptr(),
+        g["dlambda"].data_ptr(), g["dtheta"].data_ptr(),
+        g["dh0"].data_ptr() if want_dh0 else None, workspace.data_ptr(), workspace.numel(),
+        _stream_handle(stream))
+    if st != M3_OK:
+        raise M3Error(st, "m3_ssm_prefill_backward")
+    return g
 
 
 def m3_ssm_device_status(workspace: torch.Tensor, stream=None) -> int:

@@ -164,6 +164,61 @@ m3_status m3_ssm_decode_step(const m3_dims* dims, const m3_state* state, const v
   return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }
 
+size_t m3_ssm_prefill_backward_workspace(const m3_dims* dims) {
+  if (!dims || check_dims(dims, true) != M3_OK || !m3::backward_supported(*dims)) return kStatusBytes;
+  const size_t b = m3::backward_workspace(*dims).bytes;
+  return b > kStatusBytes ? b : kStatusBytes;
+}
+
+m3_status m3_ssm_prefill_backward(const m3_dims* dims, const void* x, const void* B, const void* C,
+                                  const void* dt, const float* A, const void* lambda,
+                                  const void* theta, const m3_state* h0, const void* dy,
+                                  const float* dhT, float* dx, float* dB, float* dC, float* ddt,
+                                  float* dA, float* dlambda, float* dtheta, float* dh0,
+                                  void* workspace, size_t ws_bytes, void* stream) {
+  m3_status st = check_dims(dims, true);
+  if (st != M3_OK) return st;
+  const m3_dims& d = *dims;
+  if (!m3::backward_supported(d)) return M3_ERR_SHAPE;
+  if (h0 && !state_all_or_none(h0)) return M3_ERR_ARG;
+  if (!workspace) return M3_ERR_WORKSPACE;
+  if (ws_bytes < m3_ssm_prefill_backward_workspace(dims)) return M3_ERR_WORKSPACE;
+  if (d.B == 0 || d.H == 0) return M3_OK;
+  if (!A || !dA) return M3_ERR_ARG;
+  if (d.T > 0 && (!x || !B || !C || !dt || !lambda || !theta || !dy || !dx || !dB || !dC || !ddt ||
+                  !dlambda || !dtheta))
+    return M3_ERR_ARG;
+  if (!aligned16(x) || !aligned16(B) || !aligned16(C) || !aligned16(dt) || !aligned16(A) ||
+      !aligned16(lambda) || !aligned16(theta) || !aligned16(dy) || !aligned16(dhT) ||
+      !aligned16(dx) || !aligned16(dB) || !aligned16(dC) || !aligned16(ddt) || !aligned16(dA) ||
+      !aligned16(dlambda) || !aligned16(dtheta) || !aligned16(dh0) || !aligned16(workspace))
+    return M3_ERR_ALIGN;
+  if (h0 && !state_aligned(h0)) return M3_ERR_ALIGN;
+  m3::BackwardArgs a{};
+  a.d = d;
+  a.x = x;
+  a.B = B;
+  a.C = C;
+  a.dt = dt;
+  a.A = A;
+  a.lam = lambda;
+  a.theta = theta;
+  a.h0 = (h0 && h0->h) ? *h0 : m3_state{nullptr, nullptr, nullptr, nullptr};
+  a.dy = dy;
+  a.dhT = dhT;
+  a.dx = dx;
+  a.dB = dB;
+  a.dC = dC;
+  a.ddt = ddt;
+  a.dA = dA;
+  a.dlam = dlambda;
+  a.dtheta = dtheta;
+  a.dh0 = dh0;
+  a.ws = static_cast<uint8_t*>(workspace);
+  const cudaError_t e = m3::launch_backward(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+}
+
 m3_status m3_ssd_decode_step(const m3_dims* dims, float* h, const void* x_t, const void* B_t,
                              const void* C_t, const void* dt_t, const float* A, void* y_t,
                              void* stream) {

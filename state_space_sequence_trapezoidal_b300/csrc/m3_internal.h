@@ -59,4 +59,35 @@ cudaError_t launch_prefill_recurrent(const PrefillArgs& a, cudaStream_t s);
 bool decode_supported(const m3_dims& d);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
+// Backward pass of the prefill (CUDA cores, fp32; checkpointed adjoint recurrence).
+struct BackwardArgs {
+  m3_dims d;
+  const void* x;
+  const void* B;
+  const void* C;
+  const void* dt;
+  const float* A;
+  const void* lam;
+  const void* theta;
+  m3_state h0;  // all members null for a fresh sequence
+  const void* dy;
+  const float* dhT;  // null: no gradient on the exit state
+  float* dx;
+  float* dB;
+  float* dC;
+  float* ddt;
+  float* dA;
+  float* dlam;
+  float* dtheta;
+  float* dh0;  // null: not wanted
+  uint8_t* ws;
+};
+struct BackwardWorkspace {
+  int nch, kp;              // checkpoints per sequence, padded angle count
+  size_t off_da, off_ck, bytes;
+};
+BackwardWorkspace backward_workspace(const m3_dims& d);
+bool backward_supported(const m3_dims& d);
+cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s);
+
 }  // namespace m3

@@ -130,3 +130,31 @@ def test_ssd_entry_points_reject_bad_arguments():
     assert dec(_dims(), x=None) == ARG
     assert dec(_dims(), h=8) == ALIGN
     assert dec(_dims(), y=4) == ALIGN
+
+
+def test_backward_rejects_bad_arguments():
+    lib = m3.load()
+
+    def call(d, x=16, dy=16, dx=16, dA=16, ws=16, wsb=1 << 30, dhT=None, dh0=None):
+        return lib.m3_ssm_prefill_backward(ctypes.byref(d), x, 16, 16, 16, 16, 16, 16, None, dy, dhT,
+                                           dx, 16, 16, 16, dA, 16, 16, dh0, ws, wsb, None)
+
+    assert call(_dims(N=7)) == SHAPE
+    assert call(_dims(N=256, P=64)) == SHAPE          # N P > 8192: not supported
+    assert call(_dims(), ws=None) == WS
+    assert call(_dims(), wsb=8) == WS
+    assert call(_dims(), x=None) == ARG
+    assert call(_dims(), dy=None) == ARG
+    assert call(_dims(), dA=None) == ARG
+    assert call(_dims(), dx=8) == ALIGN
+    assert call(_dims(), dhT=24) == ALIGN
+    assert call(_dims(), dh0=40) == ALIGN
+
+
+def test_backward_workspace_holds_the_checkpoints():
+    lib = m3.load()
+    d = _dims(B=8, T=4096, H=32, P=64, N=128)
+    n = lib.m3_ssm_prefill_backward_workspace(ctypes.byref(d))
+    # one N x P state (plus angles) every 16 tokens per (batch row, head)
+    assert n >= 8 * 32 * (4096 // 16) * 128 * 64 * 4
+    assert lib.m3_ssm_prefill_backward_workspace(ctypes.byref(_dims(N=256, P=64))) == 256
