@@ -17,7 +17,9 @@
 // first runs the forward recurrence and stores the state and angle every CH tokens in the
 // workspace (checkpoints); the reverse sweep then recomputes each chunk of CH tokens from its
 // checkpoint (states kept per thread, B~, C~, X, dy, sin/cos of the chunk in shared memory)
-// and walks it backwards.  Thread (p, g) owns column p of state rows g, g + G, ...; sums over
+// and walks it backwards.  Both forward passes go a chunk at a time: the chunk's inputs are
+// staged with all loads in flight, the angle and the rotation advance per pair over the chunk,
+// and the state entries then run through the chunk without a barrier.  Thread (p, g) owns column p of state rows g, g + G, ...; sums over
 // p go through a padded shared copy of G and h_t, sums over n through per-group partials; the
 // four scalar adjoints of a token are summed by one warp in a fixed order, and dA over batch
 // rows by a second kernel, so results are deterministic.
@@ -177,54 +179,79 @@ __global__ void __launch_bounds__(1024) prefill_backward_kernel(const BwdParams 
         u = to_f(pb[2 * k]);
         v = to_f(pb[2 * k + 1]);
       }
-      sB[(2 * R + r) * N + 2 * k] = c * u + s * v;  // slot 2 == slot (-1) mod 3
-      sB[(2 * R + r) * N + 2 * k + 1] = -s * u + c * v;
+      sB[r * N + 2 * k] = c * u + s * v;  // slot 0: the token before the first chunk
+      sB[r * N + 2 * k + 1] = -s * u + c * v;
     }
   }
   for (int i = tid; i < R * P; i += nth)
-    sX[2 * R * P + i] =
-        p.prevx0 ? to_f(static_cast<const Tin*>(p.prevx0)[static_cast<size_t>(bh) * R * P + i]) : 0.f;
+    sX[i] = p.prevx0 ? to_f(static_cast<const Tin*>(p.prevx0)[static_cast<size_t>(bh) * R * P + i]) : 0.f;
   __syncthreads();
 
   // ------------------------------------------------------------------ forward, checkpoints
-  // B~ and X in three slots by t mod 3: token t reads slots t and t - 1 while token t + 1
-  // writes slot t + 1, so one barrier per token suffices.
-  for (int t = 0; t < T; ++t) {
-    const int cur = t % 3, prv = (t + 2) % 3;
-    if (t % CH == 0) {
-      float* c0 = ck + static_cast<size_t>(t / CH) * (static_cast<size_t>(N) * P + p.Kp);
+  // Chunk by chunk: the chunk's raw inputs are staged in shared memory with all loads in
+  // flight together; the pair threads advance the angle and rotate B for the whole chunk; then
+  // every thread runs its own state entries through the chunk with no barrier.  Slot 0 of the
+  // B~ / X buffers holds the token before the chunk.
+  for (int j = 0; j < p.nch; ++j) {
+    const int t0 = j * CH, len = min(CH, T - t0);
+    float* c0 = ck + static_cast<size_t>(j) * (static_cast<size_t>(N) * P + p.Kp);
 #pragma unroll
-      for (int i = 0; i < kRows; ++i)
-        if (i < rows) c0[(g + i * G) * P + pcol] = h[i];
-      for (int k = tid; k < K; k += nth) c0[static_cast<size_t>(N) * P + k] = sPhi[k];
+    for (int i = 0; i < kRows; ++i)
+      if (i < rows) c0[(g + i * G) * P + pcol] = h[i];
+    for (int k = tid; k < K; k += nth) c0[static_cast<size_t>(N) * P + k] = sPhi[k];
+    if (j > 0) {  // the previous chunk's last token moves to slot 0
+      __syncthreads();
+      for (int i = tid; i < R * N; i += nth) sB[i] = sB[CH * R * N + i];
+      for (int i = tid; i < R * P; i += nth) sX[i] = sX[CH * R * P + i];
+      __syncthreads();
     }
-    const float dt = to_f(dtg[tok(t)]);
-    for (int k = tid; k < K; k += nth) {
-      const float ph = wrap(sPhi[k] + dt * to_f(thg[tok(t) * K + k]));
-      sPhi[k] = ph;
-      float s, c;
-      sincosf(ph, &s, &c);
-      for (int r = 0; r < R; ++r) {
-        const size_t o = (tok(t) * R + r) * N + 2 * k;
-        const float u = to_f(Bg[o]), v = to_f(Bg[o + 1]);
-        sB[(cur * R + r) * N + 2 * k] = c * u + s * v;
-        sB[(cur * R + r) * N + 2 * k + 1] = -s * u + c * v;
-      }
+    for (int idx = tid; idx < len * R * N; idx += nth) {
+      const int q = idx / (R * N), i = idx - q * (R * N);
+      sB[(q + 1) * R * N + i] = to_f(Bg[tok(t0 + q) * R * N + i]);
     }
-    for (int i = tid; i < R * P; i += nth) sX[cur * R * P + i] = to_f(xg[tok(t) * R * P + i]);
+    for (int idx = tid; idx < len * R * P; idx += nth) {
+      const int q = idx / (R * P), i = idx - q * (R * P);
+      sX[(q + 1) * R * P + i] = to_f(xg[tok(t0 + q) * R * P + i]);
+    }
+    for (int idx = tid; idx < len * K; idx += nth) {
+      const int q = idx / K, k = idx - q * K;
+      sTH[q * K + k] = to_f(thg[tok(t0 + q) * K + k]);
+    }
+    for (int q = tid; q < len; q += nth) {
+      sCoef[q * 5 + 3] = to_f(dtg[tok(t0 + q)]);
+      sCoef[q * 5 + 4] = to_f(lamg[tok(t0 + q)]);
+    }
     __syncthreads();
-    const float lam = to_f(lamg[tok(t)]);
-    const float alpha = expf(dt * A), beta = (1.f - lam) * dt * alpha, gamma = lam * dt;
-#pragma unroll
-    for (int i = 0; i < kRows; ++i) {
-      if (i < rows) {
-        const int n = g + i * G;
-        float pt = 0.f, ct = 0.f;
+    for (int k = tid; k < K; k += nth) {
+      float ph = sPhi[k];
+      for (int q = 0; q < len; ++q) {
+        ph = wrap(ph + sCoef[q * 5 + 3] * sTH[q * K + k]);
+        float sn, cs;
+        sincosf(ph, &sn, &cs);
         for (int r = 0; r < R; ++r) {
-          pt = fmaf(sB[(prv * R + r) * N + n], sX[(prv * R + r) * P + pcol], pt);
-          ct = fmaf(sB[(cur * R + r) * N + n], sX[(cur * R + r) * P + pcol], ct);
+          float* bq = sB + ((q + 1) * R + r) * N + 2 * k;
+          const float u = bq[0], v = bq[1];
+          bq[0] = cs * u + sn * v;
+          bq[1] = -sn * u + cs * v;
         }
-        h[i] = fmaf(alpha, h[i], fmaf(beta, pt, gamma * ct));
+      }
+      sPhi[k] = ph;
+    }
+    __syncthreads();
+    for (int q = 0; q < len; ++q) {
+      const float dt = sCoef[q * 5 + 3], lam = sCoef[q * 5 + 4];
+      const float alpha = expf(dt * A), beta = (1.f - lam) * dt * alpha, gamma = lam * dt;
+#pragma unroll
+      for (int i = 0; i < kRows; ++i) {
+        if (i < rows) {
+          const int n = g + i * G;
+          float pt = 0.f, ct = 0.f;
+          for (int r = 0; r < R; ++r) {
+            pt = fmaf(sB[(q * R + r) * N + n], sX[(q * R + r) * P + pcol], pt);
+            ct = fmaf(sB[((q + 1) * R + r) * N + n], sX[((q + 1) * R + r) * P + pcol], ct);
+          }
+          h[i] = fmaf(alpha, h[i], fmaf(beta, pt, gamma * ct));
+        }
       }
     }
   }
@@ -275,42 +302,51 @@ __global__ void __launch_bounds__(1024) prefill_backward_kernel(const BwdParams 
         v = to_f(static_cast<const Tin*>(p.prevx0)[static_cast<size_t>(bh) * R * P + i]);
       sX[i] = v;
     }
-    for (int q = 0; q < len; ++q) {
-      const int t = t0 + q;
-      const float dt = to_f(dtg[tok(t)]);
-      if (tid == 0) {
-        const float lam = to_f(lamg[tok(t)]);
-        const float alpha = expf(dt * A);
-        sCoef[q * 5 + 0] = alpha;
-        sCoef[q * 5 + 1] = (1.f - lam) * dt * alpha;
-        sCoef[q * 5 + 2] = lam * dt;
-        sCoef[q * 5 + 3] = dt;
-        sCoef[q * 5 + 4] = lam;
-      }
-      for (int k = tid; k < K; k += nth) {
-        const float th = to_f(thg[tok(t) * K + k]);
-        const float ph = wrap(sPhi[k] + dt * th);
-        sPhi[k] = ph;
-        float s, c;
-        sincosf(ph, &s, &c);
-        sCS[q * K + k] = c;
-        sSN[q * K + k] = s;
-        sTH[q * K + k] = th;
+    for (int idx = tid; idx < len * R * N; idx += nth) {
+      const int q = idx / (R * N), i = idx - q * (R * N);
+      sB[(q + 1) * R * N + i] = to_f(Bg[tok(t0 + q) * R * N + i]);
+      sC[q * R * N + i] = to_f(Cg[tok(t0 + q) * R * N + i]);
+    }
+    for (int idx = tid; idx < len * R * P; idx += nth) {
+      const int q = idx / (R * P), i = idx - q * (R * P);
+      sX[(q + 1) * R * P + i] = to_f(xg[tok(t0 + q) * R * P + i]);
+      sDy[q * R * P + i] = to_f(dyg[tok(t0 + q) * R * P + i]);
+    }
+    for (int idx = tid; idx < len * K; idx += nth) {
+      const int q = idx / K, k = idx - q * K;
+      sTH[q * K + k] = to_f(thg[tok(t0 + q) * K + k]);
+    }
+    for (int q = tid; q < len; q += nth) {
+      const float dt = to_f(dtg[tok(t0 + q)]), lam = to_f(lamg[tok(t0 + q)]);
+      const float alpha = expf(dt * A);
+      sCoef[q * 5 + 0] = alpha;
+      sCoef[q * 5 + 1] = (1.f - lam) * dt * alpha;
+      sCoef[q * 5 + 2] = lam * dt;
+      sCoef[q * 5 + 3] = dt;
+      sCoef[q * 5 + 4] = lam;
+    }
+    __syncthreads();
+    for (int k = tid; k < K; k += nth) {
+      float ph = sPhi[k];
+      for (int q = 0; q < len; ++q) {
+        ph = wrap(ph + sCoef[q * 5 + 3] * sTH[q * K + k]);
+        float sn, cs;
+        sincosf(ph, &sn, &cs);
+        sCS[q * K + k] = cs;
+        sSN[q * K + k] = sn;
         for (int r = 0; r < R; ++r) {
-          const size_t o = (tok(t) * R + r) * N + 2 * k;
-          const float bu = to_f(Bg[o]), bv = to_f(Bg[o + 1]);
-          const float cu = to_f(Cg[o]), cv = to_f(Cg[o + 1]);
-          sB[((q + 1) * R + r) * N + 2 * k] = c * bu + s * bv;
-          sB[((q + 1) * R + r) * N + 2 * k + 1] = -s * bu + c * bv;
-          sC[(q * R + r) * N + 2 * k] = c * cu + s * cv;
-          sC[(q * R + r) * N + 2 * k + 1] = -s * cu + c * cv;
+          float* bq = sB + ((q + 1) * R + r) * N + 2 * k;
+          float* cq = sC + (q * R + r) * N + 2 * k;
+          const float bu = bq[0], bv = bq[1], cu = cq[0], cv = cq[1];
+          bq[0] = cs * bu + sn * bv;
+          bq[1] = -sn * bu + cs * bv;
+          cq[0] = cs * cu + sn * cv;
+          cq[1] = -sn * cu + cs * cv;
         }
       }
-      for (int i = tid; i < R * P; i += nth) {
-        sX[(q + 1) * R * P + i] = to_f(xg[tok(t) * R * P + i]);
-        sDy[q * R * P + i] = to_f(dyg[tok(t) * R * P + i]);
-      }
-      __syncthreads();
+    }
+    __syncthreads();
+    for (int q = 0; q < len; ++q) {
       const float alpha = sCoef[q * 5 + 0], beta = sCoef[q * 5 + 1], gamma = sCoef[q * 5 + 2];
 #pragma unroll
       for (int i = 0; i < kRows; ++i) {
@@ -371,22 +407,35 @@ __global__ void __launch_bounds__(1024) prefill_backward_kernel(const BwdParams 
         redA[g * P + pcol] = pa;
       }
       __syncthreads();
-      // S1: sums over p (per (n, r)) and over n (per (p, r))
-      for (int task = tid; task < N * R; task += nth) {
-        const int n = task / R, r = task - n * R;
+      // S1: sums over p (per (n, r), eight lanes per (n, r) and a fixed shuffle tree; the loop
+      // runs over whole warps so that every lane takes part in the shuffles) and over n (per (p, r))
+      for (int t8 = tid; t8 < (N * R * 8 + 31) / 32 * 32; t8 += nth) {
+        const int task = t8 >> 3, sub = t8 & 7;
+        const bool valid = task < N * R;
+        const int n = valid ? task / R : 0, r = valid ? task - n * R : 0;
         float dc = 0.f, gx = 0.f, gxp = 0.f;
-        const float* grow = sG + n * (P + 1);
-        const float* hrow = sH + n * (P + 1);
-        for (int pp = 0; pp < P; ++pp) {
-          dc = fmaf(hrow[pp], dyt[r * P + pp], dc);
-          gx = fmaf(grow[pp], xt[r * P + pp], gx);
-          gxp = fmaf(grow[pp], xp[r * P + pp], gxp);
+        if (valid) {
+          const float* grow = sG + n * (P + 1);
+          const float* hrow = sH + n * (P + 1);
+          for (int pp = sub; pp < P; pp += 8) {
+            dc = fmaf(hrow[pp], dyt[r * P + pp], dc);
+            gx = fmaf(grow[pp], xt[r * P + pp], gx);
+            gxp = fmaf(grow[pp], xp[r * P + pp], gxp);
+          }
         }
-        sdC[r * N + n] = dc;
-        sdB[r * N + n] = fmaf(gamma, gx, dBn[r * N + n]);
-        dBn[r * N + n] = beta * gxp;
-        partBG[2 * task] = bp[r * N + n] * gxp;      // d beta
-        partBG[2 * task + 1] = bt[r * N + n] * gx;   // d gamma
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) {
+          dc += __shfl_xor_sync(0xffffffffu, dc, o);
+          gx += __shfl_xor_sync(0xffffffffu, gx, o);
+          gxp += __shfl_xor_sync(0xffffffffu, gxp, o);
+        }
+        if (valid && sub == 0) {
+          sdC[r * N + n] = dc;
+          sdB[r * N + n] = fmaf(gamma, gx, dBn[r * N + n]);
+          dBn[r * N + n] = beta * gxp;
+          partBG[2 * task] = bp[r * N + n] * gxp;      // d beta
+          partBG[2 * task + 1] = bt[r * N + n] * gx;   // d gamma
+        }
       }
       for (int task = tid; task < P * R; task += nth) {
         const int r = task / P, pp = task - r * P;
