@@ -215,6 +215,23 @@ def oracle_throughput(w, inp, budget_s: float, start: int = 0, min_slices: int =
     return tokens / spent, used, done, spent
 
 
+def oracle_single_thread(w, inp, budget_s: float):
+    """The fp64 oracle on one host thread: whole (b, h) sequences one at a time until
+    ``budget_s`` seconds.  Returns (tokens/s, sequences done, seconds)."""
+    import oracle
+
+    total = w.B * w.H
+    done, spent = 0, 0.0
+    while spent < budget_s and done < total:
+        sl = [(done // w.H, done % w.H)]
+        g = oracle.gather(inp, sl)
+        t0 = time.perf_counter()
+        oracle.scan(g["x"], g["Bm"], g["Cm"], g["dt"], g["A"], g["lam"], g["theta"], nthreads=1)
+        spent += time.perf_counter() - t0
+        done += 1
+    return done * w.T / w.H / spent, done, spent
+
+
 def run_reference(args):
     """The oracle as the reference arm: each step is a bounded sample (a batch of whole
     sequences) of the headline workload, timed on the host cores."""
@@ -607,11 +624,14 @@ def main():
     # -------------------------------------------------------------- CPU oracle baseline
     if rank == 0 and world == 1 and not args.skip_extras:
         v, used, done, spent = oracle_throughput(w, inp, budget_s=10.0)
+        v1, done1, spent1 = oracle_single_thread(w, inp, budget_s=3.0)
         line["cpu_baseline"] = {
             "value": v, "unit": "tokens/s", "cores": used, "kind": "oracle",
             "sample": (f"{done} of {w.B * w.H} (b,h) sequences x {w.T} tokens of the same "
                        f"workload, {spent:.1f} s of fp64 oracle time; tokens counted as "
-                       f"sequences x T / H")}
+                       f"sequences x T / H"),
+            "single_thread": {"value": v1, "unit": "tokens/s", "cores": 1,
+                              "sample": f"{done1} (b,h) sequences x {w.T} tokens, {spent1:.1f} s"}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     D.barrier()
