@@ -208,7 +208,8 @@ def oracle_throughput(w, inp, budget_s: float, start: int = 0, min_slices: int =
         sl = [(i // w.H, i % w.H) for i in ids]
         g = oracle.gather(inp, sl)
         t0 = time.perf_counter()
-        _, _, used = oracle.scan(g["x"], g["Bm"], g["Cm"], g["dt"], g["A"], g["lam"], g["theta"])
+        _, _, used = oracle.scan(g["x"], g["Bm"], g["Cm"], g["dt"], g["A"], g["lam"], g["theta"],
+                                 nthreads=ncores)
         spent += time.perf_counter() - t0
         done += len(sl)
     tokens = done * w.T / w.H  # a token carries all H heads
