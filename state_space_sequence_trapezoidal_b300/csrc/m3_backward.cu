@@ -66,7 +66,7 @@ struct BwdParams {
 // Shared-memory plan (floats), shared by the kernel and the host.
 struct BwdSmem {
   int sB, sC, sX, sCS, sSN, sTH, sCoef, sPhi, sG, sH, sDy, redB, redBp, redA, sdB, sdC, dBn, dxn,
-      partBG, gphi, partTh, sScal, total;
+      partBG, gphi, partTh, total;
 };
 
 __host__ __device__ inline BwdSmem bwd_smem(int N, int P, int R, int G, int CH) {
@@ -99,7 +99,6 @@ __host__ __device__ inline BwdSmem bwd_smem(int N, int P, int R, int G, int CH) 
   s.partBG = take(2 * N * R);     // d beta, d gamma partials per (n, r)
   s.gphi = take(K);               // sum_{s >= t} d phi_s
   s.partTh = take(K);
-  s.sScal = take(8);
   s.total = o;
   return s;
 }
