@@ -2,8 +2,8 @@
 """Benchmark of the Mamba-3 SSM layer core on B300: prefill and decode tokens/s, % of roofline.
 
 Headline (``value``): prefill tokens/s of the SISO 1.5B-layer workload
-(B 8, T 4096, H 32, P 64, N 128, bf16 inputs, fp32 accumulation and output),
-inputs resident in HBM.  The same line carries the dominant kernel's roofline,
+(B 8, T 4096, H 32, P 64, N 128, bf16 inputs, fp32 accumulation, y written in the
+input dtype), inputs resident in HBM; the same prefill with fp32 y is timed beside it.  The same line carries the dominant kernel's roofline,
 the fp64 CPU oracle's throughput on a bounded sample, an end-to-end number
 through the C ABI with host buffers, the decode legs (B 256 x H 32, 1000
 steps from a 512-token prefill state; SISO N 128 and MIMO R 4 N 64), the
@@ -282,6 +282,15 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--skip-extras", action="store_true", help="headline prefill only")
+    ap.add_argument("--profile-prefill", choices=["headline", "mimo", "long", "backward"],
+                    default=None,
+                    help="run only --steps plain calls of one prefill workload (the backward: "
+                         "of the headline shape cut to --profile-T tokens), for profilers; "
+                         "prints their time, no bench line")
+    ap.add_argument("--profile-B", type=int, default=0, help="batch rows of --profile-prefill "
+                    "(0: the workload's own)")
+    ap.add_argument("--profile-T", type=int, default=0, help="tokens of --profile-prefill "
+                    "(0: the workload's own)")
     ap.add_argument("--profile-decode", choices=["siso", "mimo"], default=None,
                     help="run only --decode-steps plain decode steps of one decode workload "
                          "(for profilers); prints their time, no bench line")
@@ -329,6 +338,37 @@ def main():
         D.barrier()
         return s.elapsed_time(e) / n
 
+    if args.profile_prefill:
+        name = {"headline": HEADLINE, "mimo": MIMO_PRE, "long": LONG,
+                "backward": HEADLINE}[args.profile_prefill]
+        wp = synth.WORKLOADS[name]
+        Bp, Tp = args.profile_B or wp.B, args.profile_T or wp.T
+        dp = to_dev(synth.make_inputs(Bp, Tp, wp.H, wp.P, wp.N, wp.R, wp.seed, wp.dtype), dev,
+                    torch)
+        if args.profile_prefill == "backward":
+            dyp = torch.randn(Bp, Tp, wp.H, wp.R, wp.P, dtype=torch.float32, device=dev)
+
+            def one():
+                m3.m3_ssm_prefill_backward(dp["x"], dp["B"], dp["C"], dp["dt"], dp["A"],
+                                           dp["lambda"], dp["theta"], dyp)
+        else:
+            yp = torch.empty(Bp, Tp, wp.H, wp.R, wp.P, dtype=torch.bfloat16, device=dev)
+            hp = m3.State.zeros(Bp, wp.H, wp.N, wp.P, wp.R, device=dev)
+            wsp = m3.prefill_workspace(dp["x"], dp["dt"], dp["theta"], torch.bfloat16)
+
+            def one():
+                m3.m3_ssm_prefill(dp["x"], dp["B"], dp["C"], dp["dt"], dp["A"], dp["lambda"],
+                                  dp["theta"], y=yp, hT=hp, workspace=wsp,
+                                  out_dtype=torch.bfloat16)
+
+        for _ in range(args.warmup):
+            one()
+        ms = timed(one, args.steps)
+        if rank == 0:
+            print(json.dumps({"profile_prefill": args.profile_prefill, "workload": name, "B": Bp,
+                              "T": Tp, "ms_per_call_host_launched": ms}), flush=True)
+        return 0
+
     if args.profile_decode:
         wd = synth.WORKLOADS[SISO_DEC if args.profile_decode == "siso" else MIMO_DEC]
         inp = to_dev(synth.make_inputs(wd.B, 1, wd.H, wd.P, wd.N, wd.R, wd.seed, wd.dtype), dev,
@@ -352,16 +392,18 @@ def main():
         return 0
 
     # -------------------------------------------------------------- headline prefill
+    # y in the input dtype (bf16), as the method's write-out step states; the fp32-y variant
+    # is timed beside it.
     w = synth.WORKLOADS[HEADLINE]
     inp = synth.make_inputs(w.B, w.T, w.H, w.P, w.N, w.R, D.rank_seed(w.seed, rank), w.dtype)
     d = to_dev(inp, dev, torch)
-    y = torch.empty(w.B, w.T, w.H, w.R, w.P, dtype=torch.float32, device=dev)
+    y = torch.empty(w.B, w.T, w.H, w.R, w.P, dtype=torch.bfloat16, device=dev)
     hT = m3.State.zeros(w.B, w.H, w.N, w.P, w.R, device=dev)
-    ws = m3.prefill_workspace(d["x"], d["dt"], d["theta"])
+    ws = m3.prefill_workspace(d["x"], d["dt"], d["theta"], torch.bfloat16)
 
     def prefill_step():
         m3.m3_ssm_prefill(d["x"], d["B"], d["C"], d["dt"], d["A"], d["lambda"], d["theta"], y=y,
-                          hT=hT, workspace=ws)
+                          hT=hT, workspace=ws, out_dtype=torch.bfloat16)
 
     for _ in range(args.warmup):
         prefill_step()
@@ -371,10 +413,10 @@ def main():
     ms_max = D.max_over_ranks(ms, dev)
     tokens = w.B * w.T
     value = D.aggregate_throughput(tokens, world, ms_max / 1e3)
-    pb = prefill_bytes(w)
+    pb = prefill_bytes(w, out_bytes=2)
     achieved = pb / (ms / 1e3) / 1e9
     sha = kernel_source_sha()
-    kname = "prefill_tc_kernel<128,1>"
+    kname = "prefill_tc_kernel<128,1,0,1>"
     pf = prefill_flops(w)
     in_bytes = sum(v.numel() * v.element_size() for v in d.values())
 
@@ -384,13 +426,15 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "P": w.P, "N": w.N, "R": w.R,
-                   "chunk_tokens": CHUNK_ROWS // w.R, "in_dtype": "bf16", "out_dtype": "f32",
+                   "chunk_tokens": CHUNK_ROWS // w.R, "in_dtype": "bf16", "out_dtype": "bf16",
                    "parallelism": f"replicas x{world}",
                    "l2": (f"inputs larger than L2 ({in_bytes / 1e9:.2f} GB per step vs "
                           f"{L2_BYTES / 1e6:.0f} MB)")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": measured_traffic(kname, sha),
                      "kernel": kname, "algorithmic_bytes_per_launch": pb,
+                     "bytes_per_token_head": "x 128 + B, C 512 + theta 128 + dt, lambda 4 + y 128 "
+                                             "(bf16) = 900 B, plus the exit state once",
                      "peak_source": peaks["source"],
                      "tensor_view": {"algorithmic_tflops": pf / (ms / 1e3) / 1e12,
                                      "peak": peaks["bf16_tflops"],
@@ -399,17 +443,61 @@ def main():
     }
 
     if not args.skip_extras:
+        # ---------------------------------------------------------- fp32 y at the same shape
+        y32 = torch.empty(w.B, w.T, w.H, w.R, w.P, dtype=torch.float32, device=dev)
+
+        def prefill_f32y():
+            m3.m3_ssm_prefill(d["x"], d["B"], d["C"], d["dt"], d["A"], d["lambda"], d["theta"],
+                              y=y32, hT=hT, workspace=ws)
+
+        for _ in range(3):
+            prefill_f32y()
+        ms32 = D.max_over_ranks(timed(prefill_f32y, 20), dev)
+        pb32 = prefill_bytes(w, out_bytes=4)
+        line["fp32_y"] = {"ms": ms32, "tokens_per_s": D.aggregate_throughput(tokens, world,
+                                                                             ms32 / 1e3),
+                          "algorithmic_bytes": pb32,
+                          "hbm_frac": pb32 / (ms32 / 1e3) / 1e9 / peaks["hbm_gbs"]}
+        line["gpu_launches"] += 20
+        del y32
+
         # ---------------------------------------------------------- end to end (host buffers)
+        # Pinned host inputs and outputs; the batch is cut into parts that alternate between
+        # two streams, so that one part's host-to-device copy, another's kernels and a third's
+        # device-to-host copy overlap.  Every byte still crosses the host link each step.
+        parts = 4
+        pb_rows = w.B // parts
         hin = {k: v.cpu().pin_memory() for k, v in d.items()}
         hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
         hh = torch.empty(hT.h.shape, dtype=torch.float32).pin_memory()
+        streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+        dd = {k: torch.empty_like(v) for k, v in d.items()}
+        part_dims = m3.M3Dims(pb_rows, w.T, w.H, w.P, w.N, w.R, 0, m3.M3_BF16, m3.M3_BF16)
+        wss = [m3.workspace_for(part_dims, dev) for _ in streams]
+        launches_per_part = 1 if wss[0].numel() <= 256 else 3
+        hstates = [m3.State(hT.h[i * pb_rows:(i + 1) * pb_rows], hT.phi[i * pb_rows:(i + 1) * pb_rows],
+                            hT.prev_B[i * pb_rows:(i + 1) * pb_rows],
+                            hT.prev_x[i * pb_rows:(i + 1) * pb_rows]) for i in range(parts)]
 
         def e2e_step():
-            dd = {k: v.to(dev, non_blocking=True) for k, v in hin.items()}
-            m3.m3_ssm_prefill(dd["x"], dd["B"], dd["C"], dd["dt"], dd["A"], dd["lambda"],
-                              dd["theta"], y=y, hT=hT, workspace=ws)
-            hy.copy_(y, non_blocking=True)
-            hh.copy_(hT.h, non_blocking=True)
+            cur = torch.cuda.current_stream(dev)
+            dd["A"].copy_(hin["A"], non_blocking=True)
+            for i in range(parts):
+                s_ = streams[i % 2]
+                s_.wait_stream(cur)
+                with torch.cuda.stream(s_):
+                    rows = slice(i * pb_rows, (i + 1) * pb_rows)
+                    for k, v in hin.items():
+                        if k != "A":
+                            dd[k][rows].copy_(v[rows], non_blocking=True)
+                    m3.m3_ssm_prefill(dd["x"][rows], dd["B"][rows], dd["C"][rows], dd["dt"][rows],
+                                      dd["A"], dd["lambda"][rows], dd["theta"][rows], y=y[rows],
+                                      hT=hstates[i], workspace=wss[i % 2],
+                                      out_dtype=torch.bfloat16, stream=s_)
+                    hy[rows].copy_(y[rows], non_blocking=True)
+                    hh[rows].copy_(hT.h[rows], non_blocking=True)
+            for s_ in streams:
+                cur.wait_stream(s_)
 
         for _ in range(3):
             e2e_step()
@@ -417,30 +505,33 @@ def main():
         ms_e2e = D.max_over_ranks(timed(e2e_step, ne), dev)
         line["e2e"] = {"value": D.aggregate_throughput(tokens, world, ms_e2e / 1e3),
                        "unit": "tokens/s", "h2d_bytes_per_step": in_bytes,
-                       "d2h_bytes_per_step": y.numel() * 4 + hT.h.numel() * 4,
-                       "ms_per_step": ms_e2e}
-        line["gpu_launches"] += ne
-        del hin, hy, hh
+                       "d2h_bytes_per_step": y.numel() * 2 + hT.h.numel() * 4,
+                       "ms_per_step": ms_e2e,
+                       "how": (f"batch cut into {parts} parts of {pb_rows} rows on 2 streams: "
+                               "H2D of a part, its prefill and D2H of its y and h_T overlap "
+                               "with the other parts'")}
+        line["gpu_launches"] += ne * parts * launches_per_part
+        del hin, hy, hh, dd, wss
 
         # ---------------------------------------------------------- MIMO prefill
         wm = synth.WORKLOADS[MIMO_PRE]
         dm = to_dev(synth.make_inputs(wm.B, wm.T, wm.H, wm.P, wm.N, wm.R,
                                       D.rank_seed(wm.seed, rank), wm.dtype), dev, torch)
-        ym = torch.empty(wm.B, wm.T, wm.H, wm.R, wm.P, dtype=torch.float32, device=dev)
+        ym = torch.empty(wm.B, wm.T, wm.H, wm.R, wm.P, dtype=torch.bfloat16, device=dev)
         hm = m3.State.zeros(wm.B, wm.H, wm.N, wm.P, wm.R, device=dev)
 
-        wsm = m3.prefill_workspace(dm["x"], dm["dt"], dm["theta"])
+        wsm = m3.prefill_workspace(dm["x"], dm["dt"], dm["theta"], torch.bfloat16)
 
         def fm():
             m3.m3_ssm_prefill(dm["x"], dm["B"], dm["C"], dm["dt"], dm["A"], dm["lambda"],
-                              dm["theta"], y=ym, hT=hm, workspace=wsm)
+                              dm["theta"], y=ym, hT=hm, workspace=wsm, out_dtype=torch.bfloat16)
 
         for _ in range(3):
             fm()
         msm = D.max_over_ranks(timed(fm, 20), dev)
-        bm = prefill_bytes(wm)
+        bm = prefill_bytes(wm, out_bytes=2)
         line["mimo_prefill"] = {
-            "workload": wm.name, "ms": msm,
+            "workload": wm.name, "ms": msm, "out_dtype": "bf16", "algorithmic_bytes": bm,
             "tokens_per_s": D.aggregate_throughput(wm.B * wm.T, world, msm / 1e3),
             "achieved_gbs": bm / (msm / 1e3) / 1e9, "hbm_frac": bm / (msm / 1e3) / 1e9 / peaks["hbm_gbs"],
             "algorithmic_tflops": prefill_flops(wm) / (msm / 1e3) / 1e12}
@@ -586,14 +677,15 @@ def main():
         lseed = D.rank_seed(wl.seed, rank)
         dl = to_dev(synth.make_inputs(wl.B, wl.T, wl.H, wl.P, wl.N, wl.R, lseed, wl.dtype), dev,
                     torch)
-        yl = torch.empty(wl.B, wl.T, wl.H, wl.R, wl.P, dtype=torch.float32, device=dev)
+        yl = torch.empty(wl.B, wl.T, wl.H, wl.R, wl.P, dtype=torch.bfloat16, device=dev)
         sl = m3.State.zeros(wl.B, wl.H, wl.N, wl.P, wl.R, device=dev)
 
-        wsl = m3.prefill_workspace(dl["x"], dl["dt"], dl["theta"])
+        wsl = m3.prefill_workspace(dl["x"], dl["dt"], dl["theta"], torch.bfloat16)
+        long_launches = 1 if wsl.numel() <= 256 else 3  # segmented: first pass, scan, second pass
 
         def fl():
             m3.m3_ssm_prefill(dl["x"], dl["B"], dl["C"], dl["dt"], dl["A"], dl["lambda"],
-                              dl["theta"], y=yl, hT=sl, workspace=wsl)
+                              dl["theta"], y=yl, hT=sl, workspace=wsl, out_dtype=torch.bfloat16)
 
         for _ in range(3):
             fl()
@@ -614,11 +706,12 @@ def main():
         msld = D.max_over_ranks(timed(lgraph.replay, 1), dev)
         line["long"] = {"workload": wl.name, "prefill_ms": msl,
                         "prefill_tokens_per_s": D.aggregate_throughput(wl.B * wl.T, world, msl / 1e3),
-                        "prefill_hbm_frac": prefill_bytes(wl) / (msl / 1e3) / 1e9 / peaks["hbm_gbs"],
+                        "prefill_hbm_frac": prefill_bytes(wl, 2) / (msl / 1e3) / 1e9 / peaks["hbm_gbs"],
+                        "prefill_algorithmic_bytes": prefill_bytes(wl, 2), "out_dtype": "bf16",
                         "decode_steps": wl.decode_steps,
                         "decode_us_per_step": msld / wl.decode_steps * 1e3,
                         "end_to_end_ms": msl + msld}
-        line["gpu_launches"] += 10 + wl.decode_steps
+        line["gpu_launches"] += 10 * long_launches + wl.decode_steps
 
     line["clocks"] = clocks.summary()
 

@@ -54,7 +54,7 @@ typedef enum {
   M3_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned */
   M3_ERR_CUDA = 5,        /* a CUDA launch or call failed */
   M3_ERR_TIMEOUT = 6,     /* a device-side bounded wait ran out (see m3_ssm_device_status) */
-  M3_ERR_UNSUPPORTED = 7, /* valid request this build does not implement (e.g. chunk value) */
+  M3_ERR_UNSUPPORTED = 7, /* valid request this build does not implement */
   M3_ERR_WORKSPACE = 8,   /* workspace missing or smaller than m3_ssm_prefill_workspace() */
   M3_ERR_RANGE = 9        /* an input exceeded the tensor-core path's fp16 operand range
                              (see m3_ssm_prefill; reported by m3_ssm_device_status) */
@@ -69,11 +69,13 @@ typedef struct {
   int P;              /* head dimension (multiple of 4, <= 256) */
   int N;              /* state dimension (even, <= 256); N/2 rotation pairs */
   int R;              /* MIMO rank: 1, 2, 4 or 8 (1 = SISO) */
-  int chunk;          /* prefill chunk length in tokens: 0 = the kernel's own choice.
-                         The result does not depend on it (the chunked form is the
-                         same linear map reassociated).  The bf16 tensor-core path
-                         runs 128/R tokens per chunk; any other nonzero value
-                         returns M3_ERR_UNSUPPORTED there. */
+  int chunk;          /* prefill chunk length in tokens, a hint (>= 0; 0 = the
+                         kernel's own choice).  The result does not depend on it:
+                         the chunked form is the same linear map as the recurrence,
+                         reassociated.  The bf16 tensor-core kernel always runs
+                         chunks of 128 (token, rank) rows, i.e. 128/R tokens, and
+                         the fp32 recurrent kernel runs token by token, whatever
+                         value is passed. */
   m3_dtype in_dtype;  /* x, B, C, dt, lambda, theta, prev_B, prev_x */
   m3_dtype out_dtype; /* y */
 } m3_dims;
@@ -158,7 +160,10 @@ m3_status m3_ssm_device_status(void* workspace, void* stream);
  * allocates nothing (no cudaMalloc, no cudaFree, no allocating library routine).
  *   - The first call on a device looks up the array's device address on the
  *     current device (cudaGetSymbolAddress) and caches it; make that first call
- *     before any stream capture on that device.
+ *     before any stream capture on that device.  The scratch used is that of the
+ *     device current at the call, which must be the device holding the tensors.
+ *     cudaDeviceReset invalidates the cached address: do not call this entry point
+ *     on a device after resetting it in the same process.
  *   - Each call clears the part of the array it uses (cudaMemsetAsync on
  *     `stream`) before the kernels run.
  *   - Every call on a device shares the one array and leaves its contents

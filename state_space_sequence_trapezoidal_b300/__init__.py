@@ -7,7 +7,10 @@ theta = 0) for the Mamba-2 versus Mamba-3 comparison.  This package is the thin 
 """
 from ._binding import (  # noqa: F401
     M3_BF16,
+    M3_ERR_RANGE,
     M3_ERR_TIMEOUT,
+    M3_ERR_UNSUPPORTED,
+    M3_ERR_WORKSPACE,
     M3_F32,
     M3_OK,
     M3Dims,

@@ -18,6 +18,8 @@ from . import build as _build
 
 M3_OK = 0
 M3_ERR_TIMEOUT = 6
+M3_ERR_UNSUPPORTED = 7
+M3_ERR_WORKSPACE = 8
 M3_ERR_RANGE = 9
 M3_F32, M3_BF16 = 0, 1
 _DT = {torch.float32: M3_F32, torch.bfloat16: M3_BF16}
@@ -199,22 +201,34 @@ def m3_ssm_prefill_noalloc(x, B, C, dt, A, lam, theta, h0: State | None = None, 
                            hT: State | None = None, out_dtype=torch.float32, stream=None):
     """m3_ssm_prefill without a workspace, for callers that may not allocate device
     memory: the library's own static device scratch is used instead.  ``y`` must be
-    given (this wrapper allocates nothing either).  Calls on one device share that
-    scratch, so calls that overlap on the GPU race; order them on one stream."""
+    given (this wrapper allocates nothing either).  Every tensor must sit on one device;
+    the call runs with that device current, so the scratch of that device is used.
+    Calls on one device share that scratch, so calls that overlap on the GPU race;
+    order them on one stream."""
     in_dt = x.dtype
-    _check_inputs(dict(x=x, B=B, C=C, dt=dt, lam=lam, theta=theta), in_dt)
+    dev = _check_inputs(dict(x=x, B=B, C=C, dt=dt, lam=lam, theta=theta), in_dt)
     _check_inputs(dict(A=A), torch.float32)
     d = _dims(x, dt, theta, 0, in_dt, out_dtype)
     if y.dtype != out_dtype or not y.is_contiguous() or y.numel() != d.B * d.T * d.H * d.R * d.P:
         raise ValueError("y: wrong dtype, layout or size")
+    for name, t in (("A", A), ("y", y)):
+        if t.device != dev:
+            raise ValueError(f"{name}: on {t.device}, inputs on {dev}")
+    for name, s in (("h0", h0), ("hT", hT)):
+        if s is not None and any(t.device != dev for t in (s.h, s.phi, s.prev_B, s.prev_x)):
+            raise ValueError(f"{name}: state tensors must be on {dev}")
     c0 = h0._c() if h0 is not None else None
     c1 = hT._c() if hT is not None else None
-    st = load().m3_ssm_prefill_noalloc(ctypes.byref(d), x.data_ptr(), B.data_ptr(), C.data_ptr(),
-                                       dt.data_ptr(), A.data_ptr(), lam.data_ptr(),
-                                       theta.data_ptr(),
-                                       ctypes.byref(c0) if c0 is not None else None, y.data_ptr(),
-                                       ctypes.byref(c1) if c1 is not None else None,
-                                       _stream_handle(stream))
+    # The library takes the scratch array of the CUDA device that is current during the
+    # call, so the call runs with the tensors' device current.
+    with torch.cuda.device(dev):
+        st = load().m3_ssm_prefill_noalloc(ctypes.byref(d), x.data_ptr(), B.data_ptr(),
+                                           C.data_ptr(), dt.data_ptr(), A.data_ptr(),
+                                           lam.data_ptr(), theta.data_ptr(),
+                                           ctypes.byref(c0) if c0 is not None else None,
+                                           y.data_ptr(),
+                                           ctypes.byref(c1) if c1 is not None else None,
+                                           _stream_handle(stream))
     if st != M3_OK:
         raise M3Error(st, "m3_ssm_prefill_noalloc")
     return y

@@ -111,11 +111,7 @@ m3_status prefill_common(const m3_dims* dims, const void* x, const void* B, cons
 
   // With no tokens the call only copies the entry state to the exit state.
   const bool tc = m3::prefill_tc_supported(d) && d.T > 0;
-  if (!tc) {
-    if (d.T > 0 && d.chunk != 0 && d.in_dtype == M3_BF16 && d.P == 64 && (d.N == 64 || d.N == 128))
-      return M3_ERR_UNSUPPORTED;  // tensor-core shape with a chunk length it does not run
-    if (!m3::prefill_recurrent_supported(d)) return M3_ERR_SHAPE;
-  }
+  if (!tc && !m3::prefill_recurrent_supported(d)) return M3_ERR_SHAPE;
   if (empty) return M3_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const cudaError_t e = tc ? m3::launch_prefill_tc(a, s) : m3::launch_prefill_recurrent(a, s);

@@ -18,7 +18,7 @@
 // which carries the trapezoid's previous-token term across the boundary.
 // B~, C~ are B, C rotated by the cumulative angle (Proposition 3).
 //
-// Kernel design: one CTA per (batch row, head) sequence, 14 warps with fixed roles;
+// Kernel design: one CTA per (batch row, head) sequence, 18 warps with fixed roles;
 // chunks flow through a two-stage pipeline so that loads, CUDA-core work and
 // tensor-core work of neighbouring chunks overlap:
 //   warp 0       TMA producer: raw bf16 tiles of B, C and X (128-byte swizzle) into
@@ -28,10 +28,11 @@
 //                cumulative angle, rotation of B and C in place to fp16, and the
 //                d-scaled copy of X in fp16.  theta, dt and lambda are prefetched
 //                into registers one chunk ahead.
-//   warps 10-13  epilogue (one thread per TMEM lane): mask the scores in TMEM into
-//                bf16 hi/lo pairs (GEMM2 reads them from TMEM), advance the fp32
-//                state (kept in TMEM) and write its scaled fp16 copy for GEMM3, and
-//                write y.
+//   warps 10-13  mask epilogue (one thread per TMEM lane): mask the scores in TMEM
+//                into bf16 hi/lo pairs, which GEMM2 reads from TMEM.
+//   warps 14-17  state and output epilogue (one thread per TMEM lane): advance the
+//                fp32 state (kept in TMEM), write its scaled fp16 copy for GEMM3,
+//                and write y.
 // The decay factor of a score below the diagonal 32x32 block is split as
 // 2^{l_i - l_ref} * 2^{l_ref - l_j} with l_ref the decay sum of the block's last
 // column: both factors are at most 1, so nothing overflows, and the per-column
@@ -1230,7 +1231,7 @@ TcSegments tc_segments(const m3_dims& d) {
 
 bool prefill_tc_supported(const m3_dims& d) {
   return d.in_dtype == M3_BF16 && d.P == kP && (d.N == 64 || d.N == 128) &&
-         (d.R == 1 || d.R == 2 || d.R == 4 || d.R == 8) && (d.chunk == 0 || d.chunk == kRows / d.R);
+         (d.R == 1 || d.R == 2 || d.R == 4 || d.R == 8);
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {

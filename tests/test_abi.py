@@ -62,7 +62,6 @@ def _prefill(d, ptrs=None, ws=256, h0=None, hT=None):
     (dict(N=127), SHAPE), (dict(N=0), SHAPE), (dict(N=258), SHAPE), (dict(P=6), SHAPE),
     (dict(P=0), SHAPE), (dict(R=3), SHAPE), (dict(B=-1), SHAPE), (dict(T=-1), SHAPE),
     (dict(chunk=-1), SHAPE), (dict(in_dtype=7), DTYPE), (dict(out_dtype=5), DTYPE),
-    (dict(chunk=64), UNSUP),
 ])
 def test_prefill_rejects_bad_dims(kw, code):
     assert _prefill(_dims(**kw)) == code
@@ -124,7 +123,6 @@ def test_ssd_entry_points_reject_bad_arguments():
     assert pre(_dims(), y=8) == ALIGN
     assert pre(_dims(), h0=24) == ALIGN
     assert pre(_dims(), hT=40) == ALIGN
-    assert pre(_dims(chunk=64)) == UNSUP
     assert dec(_dims(R=4)) == SHAPE
     assert dec(_dims(), h=None) == ARG
     assert dec(_dims(), x=None) == ARG
