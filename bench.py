@@ -513,6 +513,33 @@ def main():
         line["gpu_launches"] += ne * parts * launches_per_part
         del hin, hy, hh, dd, wss
 
+        # ---------------------------------------------------------- fused BCNorm + bias prologue
+        # The headline prefill on raw B, C projection outputs, normalised, weighted and
+        # biased inside the kernel, against the plain prefill above (inputs already
+        # normalised).  Same HBM bytes (the parameters are 1 KB).
+        prm = synth.make_bcnorm_params(w.N, w.H, w.R, D.rank_seed(w.seed, rank) + 7)
+        raw = synth.make_raw_bc({k: inp[k] for k in ("B", "C")}, D.rank_seed(w.seed, rank) + 8)
+        rb = {k: torch.from_numpy(raw[k]).to(dev, torch.bfloat16) for k in ("B", "C")}
+        norm = m3.BCNorm(**{k: torch.from_numpy(prm[k]).to(dev, torch.bfloat16)
+                            for k in ("B_weight", "B_bias", "C_weight", "C_bias")}, eps=prm["eps"])
+
+        def prefill_bcnorm():
+            m3.m3_ssm_prefill_bcnorm(d["x"], rb["B"], rb["C"], d["dt"], d["A"], d["lambda"],
+                                     d["theta"], norm, y=y, hT=hT, workspace=ws,
+                                     out_dtype=torch.bfloat16)
+
+        for _ in range(3):
+            prefill_bcnorm()
+        msn = D.max_over_ranks(timed(prefill_bcnorm, 20), dev)
+        line["bcnorm"] = {"workload": w.name, "fused_ms": msn, "plain_ms": ms_max,
+                          "fused_over_plain": msn / ms_max,
+                          "tokens_per_s": D.aggregate_throughput(tokens, world, msn / 1e3),
+                          "hbm_frac": pb / (msn / 1e3) / 1e9 / peaks["hbm_gbs"],
+                          "note": "raw B, C in; RMS norm over N, weight, per-head bias applied "
+                                  "in the transform warps"}
+        line["gpu_launches"] += 20
+        del rb, raw
+
         # ---------------------------------------------------------- MIMO prefill
         wm = synth.WORKLOADS[MIMO_PRE]
         dm = to_dev(synth.make_inputs(wm.B, wm.T, wm.H, wm.P, wm.N, wm.R,

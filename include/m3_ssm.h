@@ -182,6 +182,57 @@ m3_status m3_ssm_prefill_noalloc(const m3_dims* dims, const void* x, const void*
                                  const m3_state* hT, void* stream);
 
 /*
+ * BCNorm and the B, C biases fused into the SSM core (paper section 3.4, "BC / QK
+ * normalisation": an RMS normalisation right after the B and C projections, in the manner
+ * of QKNorm; "B, C bias": a learnable, head-specific, channel-wise bias added after the
+ * normalisation).  The pages give no formula; this library reads it as
+ *
+ *   B_t[:, r] = Braw_t[:, r] / sqrt(mean_n Braw_t[n, r]^2 + eps) * B_weight + B_bias[h]
+ *
+ * per (token, head, rank) vector of N state entries, likewise for C with its own weight and
+ * bias, and the result feeds the recurrence above in place of B and C.
+ *
+ *   B_weight, C_weight  [N] in the input dtype, shared by heads and ranks; NULL = all ones.
+ *   B_bias,   C_bias    [H][N] in the input dtype, shared by ranks; NULL = all zeros.
+ *   eps                 > 0 (and finite), added to the mean square.
+ */
+typedef struct {
+  const void* B_weight;
+  const void* B_bias;
+  const void* C_weight;
+  const void* C_bias;
+  float eps;
+} m3_bc_norm;
+
+/*
+ * m3_ssm_prefill on the raw projection outputs: B and C are the [B][T][H][R][N] values
+ * before BCNorm and the biases, which the kernels apply on the fly (the normalised B and C
+ * never go through device memory).  The state keeps the raw previous token: h0->prev_B and
+ * hT->prev_B hold the raw B of the last token, normalised again with `norm` when its
+ * trapezoid term is folded in, so continuation calls must pass the same `norm`.
+ * Every other argument, the workspace (sized by m3_ssm_prefill_workspace for the same dims),
+ * the supported shapes and the error behaviour are those of m3_ssm_prefill; `norm` must not
+ * be NULL (M3_ERR_ARG), eps must be > 0 and finite (M3_ERR_ARG), and the four parameter
+ * pointers must be 16-byte aligned or NULL (M3_ERR_ALIGN).
+ */
+m3_status m3_ssm_prefill_bcnorm(const m3_dims* dims, const void* x, const void* B_raw,
+                                const void* C_raw, const void* dt, const float* A,
+                                const void* lambda, const void* theta, const m3_bc_norm* norm,
+                                const m3_state* h0, void* y, const m3_state* hT, void* workspace,
+                                size_t ws_bytes, void* stream);
+
+/*
+ * m3_ssm_decode_step on the raw projection outputs B_t, C_t [B][H][R][N], with BCNorm and
+ * the biases applied in the step's prologue.  state->prev_B holds the raw previous B (see
+ * m3_ssm_prefill_bcnorm) and receives the raw B_t.  Arguments and errors as
+ * m3_ssm_decode_step, and `norm` as m3_ssm_prefill_bcnorm.
+ */
+m3_status m3_ssm_decode_step_bcnorm(const m3_dims* dims, const m3_state* state, const void* x_t,
+                                    const void* B_raw_t, const void* C_raw_t, const void* dt_t,
+                                    const float* A, const void* lambda_t, const void* theta_t,
+                                    const m3_bc_norm* norm, void* y_t, void* stream);
+
+/*
  * The Mamba-2 special case of the same layer core (paper section 2, Eq. (4), the
  * exponential-Euler rule that Mamba-1 and Mamba-2 use, and Remark 5: the mask keeps
  * only its diagonal weights), for the Mamba-2 versus Mamba-3 comparison of Table 6:

@@ -13,6 +13,8 @@ from ._binding import (  # noqa: F401
     M3_ERR_WORKSPACE,
     M3_F32,
     M3_OK,
+    BCNorm,
+    M3BcNorm,
     M3Dims,
     M3Error,
     M3State,
@@ -22,9 +24,11 @@ from ._binding import (  # noqa: F401
     m3_ssd_decode_step,
     m3_ssd_prefill,
     m3_ssm_decode_step,
+    m3_ssm_decode_step_bcnorm,
     m3_ssm_device_status,
     m3_ssm_prefill,
     m3_ssm_prefill_backward,
+    m3_ssm_prefill_bcnorm,
     m3_ssm_prefill_noalloc,
     m3_ssm_prefill_workspace,
     prefill_workspace,

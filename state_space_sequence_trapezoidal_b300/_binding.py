@@ -35,6 +35,12 @@ class M3State(ctypes.Structure):
                 ("prev_x", ctypes.c_void_p)]
 
 
+class M3BcNorm(ctypes.Structure):
+    _fields_ = [("B_weight", ctypes.c_void_p), ("B_bias", ctypes.c_void_p),
+                ("C_weight", ctypes.c_void_p), ("C_bias", ctypes.c_void_p),
+                ("eps", ctypes.c_float)]
+
+
 class M3Error(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -67,6 +73,13 @@ def load() -> ctypes.CDLL:
             lib.m3_ssm_prefill_noalloc.restype = ctypes.c_int
             lib.m3_ssm_decode_step.argtypes = [dp, sp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
             lib.m3_ssm_decode_step.restype = ctypes.c_int
+            np_ = ctypes.POINTER(M3BcNorm)
+            lib.m3_ssm_prefill_bcnorm.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, np_, sp, vp, sp,
+                                                  vp, sz, vp]
+            lib.m3_ssm_prefill_bcnorm.restype = ctypes.c_int
+            lib.m3_ssm_decode_step_bcnorm.argtypes = [dp, sp, vp, vp, vp, vp, vp, vp, vp, np_, vp,
+                                                      vp]
+            lib.m3_ssm_decode_step_bcnorm.restype = ctypes.c_int
             lib.m3_ssm_prefill_backward_workspace.argtypes = [dp]
             lib.m3_ssm_prefill_backward_workspace.restype = sz
             lib.m3_ssm_prefill_backward.argtypes = [dp] + [vp] * 7 + [sp] + [vp] * 10 + [vp, sz, vp]
@@ -117,6 +130,33 @@ class State:
                 raise ValueError("state tensors must be contiguous")
         return M3State(self.h.data_ptr(), self.phi.data_ptr(), self.prev_B.data_ptr(),
                        self.prev_x.data_ptr())
+
+
+@dataclass
+class BCNorm:
+    """BCNorm and the B, C biases applied by the *_bcnorm entry points: per (token, head,
+    rank) vector v of N raw projection outputs, v / sqrt(mean(v^2) + eps) * weight + bias[h].
+    Weights [N] and biases [H, N] in the input dtype, on the device; None = ones / zeros."""
+
+    B_weight: torch.Tensor | None = None
+    B_bias: torch.Tensor | None = None
+    C_weight: torch.Tensor | None = None
+    C_bias: torch.Tensor | None = None
+    eps: float = 1e-6
+
+    def _c(self, dtype, device, N: int, H: int) -> M3BcNorm:
+        ptrs = []
+        for name, shape in (("B_weight", (N,)), ("B_bias", (H, N)), ("C_weight", (N,)),
+                            ("C_bias", (H, N))):
+            t = getattr(self, name)
+            if t is None:
+                ptrs.append(None)
+                continue
+            if (t.dtype != dtype or t.device != device or not t.is_contiguous()
+                    or tuple(t.shape) != shape):
+                raise ValueError(f"{name}: {dtype} {list(shape)} contiguous on {device} expected")
+            ptrs.append(t.data_ptr())
+        return M3BcNorm(*ptrs, float(self.eps))
 
 
 def _stream_handle(stream) -> ctypes.c_void_p:
@@ -195,6 +235,58 @@ def m3_ssm_prefill(x, B, C, dt, A, lam, theta, h0: State | None = None, *, y=Non
     if st != M3_OK:
         raise M3Error(st, "m3_ssm_prefill")
     return y
+
+
+def m3_ssm_prefill_bcnorm(x, B_raw, C_raw, dt, A, lam, theta, norm: BCNorm,
+                          h0: State | None = None, *, y=None, hT: State | None = None,
+                          workspace=None, chunk: int = 0, out_dtype=torch.float32, stream=None):
+    """m3_ssm_prefill on raw B, C projection outputs, with BCNorm and the biases (``norm``)
+    applied inside the kernels.  The state's prev_B holds the raw previous B."""
+    in_dt = x.dtype
+    dev = _check_inputs(dict(x=x, B=B_raw, C=C_raw, dt=dt, lam=lam, theta=theta), in_dt)
+    _check_inputs(dict(A=A), torch.float32)
+    d = _dims(x, dt, theta, chunk, in_dt, out_dtype)
+    nc = norm._c(in_dt, dev, d.N, d.H)
+    if y is None:
+        y = torch.empty(d.B, d.T, d.H, d.R, d.P, dtype=out_dtype, device=dev)
+    elif y.dtype != out_dtype or not y.is_contiguous() or y.numel() != d.B * d.T * d.H * d.R * d.P:
+        raise ValueError("y: wrong dtype, layout or size")
+    if workspace is None:
+        workspace = workspace_for(d, dev)
+    c0 = h0._c() if h0 is not None else None
+    c1 = hT._c() if hT is not None else None
+    st = load().m3_ssm_prefill_bcnorm(ctypes.byref(d), x.data_ptr(), B_raw.data_ptr(),
+                                      C_raw.data_ptr(), dt.data_ptr(), A.data_ptr(),
+                                      lam.data_ptr(), theta.data_ptr(), ctypes.byref(nc),
+                                      ctypes.byref(c0) if c0 is not None else None, y.data_ptr(),
+                                      ctypes.byref(c1) if c1 is not None else None,
+                                      workspace.data_ptr(), workspace.numel(),
+                                      _stream_handle(stream))
+    if st != M3_OK:
+        raise M3Error(st, "m3_ssm_prefill_bcnorm")
+    return y
+
+
+def m3_ssm_decode_step_bcnorm(state: State, x_t, B_raw_t, C_raw_t, dt_t, A, lam_t, theta_t,
+                              norm: BCNorm, *, y_t=None, out_dtype=torch.float32, stream=None):
+    """m3_ssm_decode_step on raw B_t, C_t, with BCNorm and the biases applied in the step's
+    prologue.  The state's prev_B holds (and receives) the raw B."""
+    in_dt = x_t.dtype
+    dev = _check_inputs(dict(x_t=x_t, B_t=B_raw_t, C_t=C_raw_t, dt_t=dt_t, lam_t=lam_t,
+                             theta_t=theta_t), in_dt)
+    _check_inputs(dict(A=A), torch.float32)
+    d = _dims(x_t, dt_t, theta_t, 0, in_dt, out_dtype, prefill=False)
+    nc = norm._c(in_dt, dev, d.N, d.H)
+    if y_t is None:
+        y_t = torch.empty(d.B, d.H, d.R, d.P, dtype=out_dtype, device=dev)
+    c = state._c()
+    st = load().m3_ssm_decode_step_bcnorm(ctypes.byref(d), ctypes.byref(c), x_t.data_ptr(),
+                                          B_raw_t.data_ptr(), C_raw_t.data_ptr(), dt_t.data_ptr(),
+                                          A.data_ptr(), lam_t.data_ptr(), theta_t.data_ptr(),
+                                          ctypes.byref(nc), y_t.data_ptr(), _stream_handle(stream))
+    if st != M3_OK:
+        raise M3Error(st, "m3_ssm_decode_step_bcnorm")
+    return y_t
 
 
 def m3_ssm_prefill_noalloc(x, B, C, dt, A, lam, theta, h0: State | None = None, *, y,

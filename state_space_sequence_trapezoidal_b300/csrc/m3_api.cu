@@ -37,6 +37,16 @@ bool state_aligned(const m3_state* s) {
   return aligned16(s->h) && aligned16(s->phi) && aligned16(s->prev_B) && aligned16(s->prev_x);
 }
 
+// BCNorm parameters: eps > 0 and finite; parameter pointers 16-byte aligned or null.
+m3_status check_norm(const m3_bc_norm* n) {
+  if (!n) return M3_ERR_ARG;
+  if (!(n->eps > 0.f) || !(n->eps < 3.0e38f)) return M3_ERR_ARG;
+  if (!aligned16(n->B_weight) || !aligned16(n->B_bias) || !aligned16(n->C_weight) ||
+      !aligned16(n->C_bias))
+    return M3_ERR_ALIGN;
+  return M3_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -73,9 +83,11 @@ namespace {
 m3_status prefill_common(const m3_dims* dims, const void* x, const void* B, const void* C,
                          const void* dt, const float* A, const void* lambda, const void* theta,
                          const m3_state* h0, void* y, const m3_state* hT, void* workspace,
-                         size_t ws_bytes, void* stream, bool ssd) {
+                         size_t ws_bytes, void* stream, bool ssd, const m3_bc_norm* norm = nullptr,
+                         bool with_norm = false) {
   m3_status st = check_dims(dims, true);
   if (st != M3_OK) return st;
+  if (with_norm && (st = check_norm(norm)) != M3_OK) return st;
   const m3_dims& d = *dims;
   if (ssd && d.R != 1) return M3_ERR_SHAPE;
   if (!ssd && h0 && !state_all_or_none(h0)) return M3_ERR_ARG;
@@ -108,6 +120,7 @@ m3_status prefill_common(const m3_dims* dims, const void* x, const void* B, cons
   a.ws = static_cast<uint8_t*>(workspace);
   if (!a.h0.h) a.h0 = m3_state{nullptr, nullptr, nullptr, nullptr};
   if (!a.hT.h) a.hT = m3_state{nullptr, nullptr, nullptr, nullptr};
+  a.norm = with_norm ? norm : nullptr;
 
   // With no tokens the call only copies the entry state to the exit state.
   const bool tc = m3::prefill_tc_supported(d) && d.T > 0;
@@ -115,6 +128,34 @@ m3_status prefill_common(const m3_dims* dims, const void* x, const void* B, cons
   if (empty) return M3_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const cudaError_t e = tc ? m3::launch_prefill_tc(a, s) : m3::launch_prefill_recurrent(a, s);
+  return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+}
+
+}  // namespace
+
+namespace {
+
+m3_status decode_common(const m3_dims* dims, const m3_state* state, const void* x_t,
+                        const void* B_t, const void* C_t, const void* dt_t, const float* A,
+                        const void* lambda_t, const void* theta_t, void* y_t, void* stream,
+                        const m3_bc_norm* norm, bool with_norm) {
+  m3_status st = check_dims(dims, false);
+  if (st != M3_OK) return st;
+  if (with_norm && (st = check_norm(norm)) != M3_OK) return st;
+  const m3_dims& d = *dims;
+  if (!state) return M3_ERR_ARG;
+  if (!m3::decode_supported(d)) return M3_ERR_SHAPE;
+  if (d.B == 0 || d.H == 0) return M3_OK;
+  if (!state->h || !state->phi || !state->prev_B || !state->prev_x || !x_t || !B_t || !C_t ||
+      !dt_t || !A || !lambda_t || !theta_t || !y_t)
+    return M3_ERR_ARG;
+  if (!state_aligned(state) || !aligned16(x_t) || !aligned16(B_t) || !aligned16(C_t) ||
+      !aligned16(dt_t) || !aligned16(A) || !aligned16(lambda_t) || !aligned16(theta_t) ||
+      !aligned16(y_t))
+    return M3_ERR_ALIGN;
+  m3::DecodeArgs a{d, *state, x_t, B_t, C_t, dt_t, A, lambda_t, theta_t, y_t,
+                   with_norm ? norm : nullptr};
+  const cudaError_t e = m3::launch_decode(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }
 
@@ -130,6 +171,15 @@ m3_status m3_ssm_prefill(const m3_dims* dims, const void* x, const void* B, cons
                         stream, false);
 }
 
+m3_status m3_ssm_prefill_bcnorm(const m3_dims* dims, const void* x, const void* B_raw,
+                                const void* C_raw, const void* dt, const float* A,
+                                const void* lambda, const void* theta, const m3_bc_norm* norm,
+                                const m3_state* h0, void* y, const m3_state* hT, void* workspace,
+                                size_t ws_bytes, void* stream) {
+  return prefill_common(dims, x, B_raw, C_raw, dt, A, lambda, theta, h0, y, hT, workspace,
+                        ws_bytes, stream, false, norm, true);
+}
+
 m3_status m3_ssd_prefill(const m3_dims* dims, const void* x, const void* B, const void* C,
                          const void* dt, const float* A, const float* h0, void* y, float* hT,
                          void* workspace, size_t ws_bytes, void* stream) {
@@ -139,25 +189,20 @@ m3_status m3_ssd_prefill(const m3_dims* dims, const void* x, const void* B, cons
                         hT ? &s1 : nullptr, workspace, ws_bytes, stream, true);
 }
 
+
 m3_status m3_ssm_decode_step(const m3_dims* dims, const m3_state* state, const void* x_t,
                              const void* B_t, const void* C_t, const void* dt_t, const float* A,
                              const void* lambda_t, const void* theta_t, void* y_t, void* stream) {
-  m3_status st = check_dims(dims, false);
-  if (st != M3_OK) return st;
-  const m3_dims& d = *dims;
-  if (!state) return M3_ERR_ARG;
-  if (!m3::decode_supported(d)) return M3_ERR_SHAPE;
-  if (d.B == 0 || d.H == 0) return M3_OK;
-  if (!state->h || !state->phi || !state->prev_B || !state->prev_x || !x_t || !B_t || !C_t ||
-      !dt_t || !A || !lambda_t || !theta_t || !y_t)
-    return M3_ERR_ARG;
-  if (!state_aligned(state) || !aligned16(x_t) || !aligned16(B_t) || !aligned16(C_t) ||
-      !aligned16(dt_t) || !aligned16(A) || !aligned16(lambda_t) || !aligned16(theta_t) ||
-      !aligned16(y_t))
-    return M3_ERR_ALIGN;
-  m3::DecodeArgs a{d, *state, x_t, B_t, C_t, dt_t, A, lambda_t, theta_t, y_t};
-  const cudaError_t e = m3::launch_decode(a, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
+  return decode_common(dims, state, x_t, B_t, C_t, dt_t, A, lambda_t, theta_t, y_t, stream,
+                       nullptr, false);
+}
+
+m3_status m3_ssm_decode_step_bcnorm(const m3_dims* dims, const m3_state* state, const void* x_t,
+                                    const void* B_raw_t, const void* C_raw_t, const void* dt_t,
+                                    const float* A, const void* lambda_t, const void* theta_t,
+                                    const m3_bc_norm* norm, void* y_t, void* stream) {
+  return decode_common(dims, state, x_t, B_raw_t, C_raw_t, dt_t, A, lambda_t, theta_t, y_t,
+                       stream, norm, true);
 }
 
 size_t m3_ssm_prefill_backward_workspace(const m3_dims* dims) {
@@ -228,7 +273,7 @@ m3_status m3_ssd_decode_step(const m3_dims* dims, float* h, const void* x_t, con
       !aligned16(A) || !aligned16(y_t))
     return M3_ERR_ALIGN;
   m3::DecodeArgs a{d, m3_state{h, nullptr, nullptr, nullptr}, x_t, B_t, C_t, dt_t, A, nullptr,
-                   nullptr, y_t};
+                   nullptr, y_t, nullptr};
   const cudaError_t e = m3::launch_decode(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? M3_OK : M3_ERR_CUDA;
 }

@@ -36,7 +36,49 @@ struct DecodeParams {
   const void* theta;
   void* y;
   int H, N, P;
+  // BCNorm + biases (section 3.4) of B_t, C_t and the stored raw previous B, when norm != 0:
+  // weights [N] (null: ones), biases [H][N] (null: zeros), in the input dtype.
+  int norm;
+  const void* nwB;
+  const void* nbB;
+  const void* nwC;
+  const void* nbC;
+  float neps;
 };
+
+// 1 / RMS of each of the rows B_t[:, r], C_t[:, r], prev_B[:, r] (r < R) of this (b, h), into
+// s_inv[3R]; a fixed summation order, so the result does not vary from run to run.  Whole
+// warps each take one row; a block that is not a whole number of warps uses one thread per
+// row.  Ends with a barrier.
+template <typename Tin>
+__device__ void row_inv_rms(const Tin* Bt, const Tin* Ct, const Tin* Bp, int R, int N, float eps,
+                            float* s_inv) {
+  if ((blockDim.x & 31) == 0) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    for (int j = warp; j < 3 * R; j += nwarps) {
+      const Tin* row = (j < R ? Bt : j < 2 * R ? Ct : Bp) + static_cast<size_t>(j % R) * N;
+      float ss = 0.f;
+      for (int n = lane; n < N; n += 32) {
+        const float v = to_f(row[n]);
+        ss = fmaf(v, v, ss);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) s_inv[j] = rsqrtf(fmaf(ss, 1.f / N, eps));
+    }
+  } else {
+    for (int j = threadIdx.x; j < 3 * R; j += blockDim.x) {
+      const Tin* row = (j < R ? Bt : j < 2 * R ? Ct : Bp) + static_cast<size_t>(j % R) * N;
+      float ss = 0.f;
+      for (int n = 0; n < N; ++n) {
+        const float v = to_f(row[n]);
+        ss = fmaf(v, v, ss);
+      }
+      s_inv[j] = rsqrtf(fmaf(ss, 1.f / N, eps));
+    }
+  }
+  __syncthreads();
+}
 
 // R consecutive floats of one state row (rank-major factors stored [N][R]).
 template <int R>
@@ -98,6 +140,7 @@ __global__ void __launch_bounds__(MAXT, DecodeOcc<R, MAXT>::kMinBlocks) decode_s
   float* sxp = sx + R * P;       // [R][P] X_{t-1}
   float* red = sxp + R * P;      // [RG][R][P] partial outputs
   float* sphi = red + RG * R * P; // [K] advanced angle
+  float* sinv = sphi + K;         // [3R] BCNorm 1/RMS of B_t, C_t, prev_B rows
 
   const Tin* Bt = static_cast<const Tin*>(p.B);
   const Tin* Ct = static_cast<const Tin*>(p.C);
@@ -124,6 +167,13 @@ __global__ void __launch_bounds__(MAXT, DecodeOcc<R, MAXT>::kMinBlocks) decode_s
     }
     __syncthreads();
   }
+  const Tin* nwB = static_cast<const Tin*>(p.nwB);
+  const Tin* nbB = p.nbB ? static_cast<const Tin*>(p.nbB) + static_cast<size_t>(head) * N : nullptr;
+  const Tin* nwC = static_cast<const Tin*>(p.nwC);
+  const Tin* nbC = p.nbC ? static_cast<const Tin*>(p.nbC) + static_cast<size_t>(head) * N : nullptr;
+  if (kRot && p.norm)
+    row_inv_rms<Tin>(Bt + static_cast<size_t>(bh) * R * N, Ct + static_cast<size_t>(bh) * R * N,
+                     prevB + static_cast<size_t>(bh) * R * N, R, N, p.neps, sinv);
   for (int i = threadIdx.x; kRot && (i < R * K || i < R * P); i += blockDim.x) {
     const bool rot = i < R * K, cpy = i < R * P;
     const int r = rot ? i / K : 0, k = rot ? i - r * K : 0;
@@ -150,7 +200,21 @@ __global__ void __launch_bounds__(MAXT, DecodeOcc<R, MAXT>::kMinBlocks) decode_s
       float s0, c0, s1, c1;
       __sincosf(fmaf(-6.283185307179586f, rintf(ph0 * 0.15915494309189535f), ph0), &s0, &c0);
       __sincosf(fmaf(-6.283185307179586f, rintf(ph1 * 0.15915494309189535f), ph1), &s1, &c1);
-      const float bu = to_f(bu_raw), bv = to_f(bv_raw);
+      float bu = to_f(bu_raw), bv = to_f(bv_raw);
+      if (p.norm) {  // BCNorm and bias before the rotation; prev_B is stored raw
+        const int n0 = 2 * k, n1 = 2 * k + 1;
+        const float wb0 = nwB ? to_f(nwB[n0]) : 1.f, wb1 = nwB ? to_f(nwB[n1]) : 1.f;
+        const float bb0 = nbB ? to_f(nbB[n0]) : 0.f, bb1 = nbB ? to_f(nbB[n1]) : 0.f;
+        const float wc0 = nwC ? to_f(nwC[n0]) : 1.f, wc1 = nwC ? to_f(nwC[n1]) : 1.f;
+        const float bc0 = nbC ? to_f(nbC[n0]) : 0.f, bc1 = nbC ? to_f(nbC[n1]) : 0.f;
+        const float ib = sinv[r], ic = sinv[R + r], ip = sinv[2 * R + r];
+        bu = fmaf(bu * ib, wb0, bb0);
+        bv = fmaf(bv * ib, wb1, bb1);
+        cu = fmaf(cu * ic, wc0, bc0);
+        cv = fmaf(cv * ic, wc1, bc1);
+        pu = fmaf(pu * ip, wb0, bb0);
+        pv = fmaf(pv * ip, wb1, bb1);
+      }
       sBp[(2 * k) * R + r] = c0 * pu + s0 * pv;
       sBp[(2 * k + 1) * R + r] = -s0 * pu + c0 * pv;
       sBt[(2 * k) * R + r] = c1 * bu + s1 * bv;
@@ -224,7 +288,10 @@ template <typename Tin, typename Tout, int R, bool kRot>
 cudaError_t launch_r(const DecodeArgs& a, cudaStream_t s, int threads, int vpt) {
   const m3_dims& d = a.d;
   DecodeParams p{a.s.h, a.s.phi, a.s.prev_B, a.s.prev_x, a.x, a.B, a.C, a.dt, a.A, a.lam, a.theta,
-                 a.y, d.H, d.N, d.P};
+                 a.y, d.H, d.N, d.P, a.norm ? 1 : 0,
+                 a.norm ? a.norm->B_weight : nullptr, a.norm ? a.norm->B_bias : nullptr,
+                 a.norm ? a.norm->C_weight : nullptr, a.norm ? a.norm->C_bias : nullptr,
+                 a.norm ? a.norm->eps : 1.f};
   const int RG = threads / (d.P / 2);
   const size_t smem = smem_bytes(d, RG);
   const dim3 grid(static_cast<unsigned>(d.B) * static_cast<unsigned>(d.H));
@@ -256,7 +323,7 @@ cudaError_t launch_r(const DecodeArgs& a, cudaStream_t s, int threads, int vpt) 
 }
 
 size_t smem_bytes(const m3_dims& d, int RG) {
-  return sizeof(float) * (3 * d.R * d.N + 2 * d.R * d.P + RG * d.R * d.P + d.N / 2);
+  return sizeof(float) * (3 * d.R * d.N + 2 * d.R * d.P + RG * d.R * d.P + d.N / 2 + 3 * d.R);
 }
 
 // Each thread keeps VPT in {1,2,4,8,16,32} float2 of state (VPT divides N), so
@@ -296,7 +363,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   const bool bf_in = a.d.in_dtype == M3_BF16, bf_out = a.d.out_dtype == M3_BF16;
   // No theta: the Mamba-2 special case, SISO only (state h alone).
   if (!a.theta) {
-    if (a.d.R != 1 || a.lam || a.s.phi || a.s.prev_B || a.s.prev_x) return cudaErrorInvalidValue;
+    if (a.d.R != 1 || a.lam || a.s.phi || a.s.prev_B || a.s.prev_x || a.norm)
+      return cudaErrorInvalidValue;
     if (bf_in && bf_out) return launch_r<__nv_bfloat16, __nv_bfloat16, 1, false>(a, s, threads, vpt);
     if (bf_in) return launch_r<__nv_bfloat16, float, 1, false>(a, s, threads, vpt);
     if (bf_out) return launch_r<float, __nv_bfloat16, 1, false>(a, s, threads, vpt);

@@ -24,6 +24,7 @@ struct PrefillArgs {
   m3_state hT;  // all members null when no exit state is wanted
   unsigned* status;  // device status word (first bytes of the workspace)
   uint8_t* ws;       // the workspace (status word first)
+  const m3_bc_norm* norm;  // BCNorm + biases applied to B and C on the fly, or null
 };
 
 struct DecodeArgs {
@@ -37,6 +38,7 @@ struct DecodeArgs {
   const void* lam;
   const void* theta;
   void* y;
+  const m3_bc_norm* norm;  // BCNorm + biases applied to B_t, C_t and prev_B, or null
 };
 
 // Tensor-core (tcgen05) chunked prefill: bf16 inputs, P = 64, N in {64, 128}, R in {1,2,4,8}.

@@ -45,7 +45,47 @@ struct RecParams {
   void* prevBT;
   void* prevxT;
   int T, H, N, P, R, G;
+  // BCNorm + biases (section 3.4) of B, C and the stored raw previous B, when norm != 0:
+  // weights [N] (null: ones), biases [H][N] (null: zeros), in the input dtype.
+  int norm;
+  const void* nwB;
+  const void* nbB;
+  const void* nwC;
+  const void* nbC;
+  float neps;
 };
+
+// 1 / RMS over the N entries of each of `rows` rows (row j starts at src(j)), into s_inv[j],
+// in a fixed summation order.  Whole warps take one row each; a block that is not a whole
+// number of warps uses one thread per row.  Ends with a barrier.
+template <typename Tin, typename RowFn>
+__device__ void rows_inv_rms(RowFn src, int rows, int N, float eps, float* s_inv) {
+  if ((blockDim.x & 31) == 0) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    for (int j = warp; j < rows; j += nwarps) {
+      const Tin* row = src(j);
+      float ss = 0.f;
+      for (int n = lane; n < N; n += 32) {
+        const float v = to_f(row[n]);
+        ss = fmaf(v, v, ss);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) s_inv[j] = rsqrtf(fmaf(ss, 1.f / N, eps));
+    }
+  } else {
+    for (int j = threadIdx.x; j < rows; j += blockDim.x) {
+      const Tin* row = src(j);
+      float ss = 0.f;
+      for (int n = 0; n < N; ++n) {
+        const float v = to_f(row[n]);
+        ss = fmaf(v, v, ss);
+      }
+      s_inv[j] = rsqrtf(fmaf(ss, 1.f / N, eps));
+    }
+  }
+  __syncthreads();
+}
 
 template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(1024) prefill_recurrent_kernel(const RecParams p) {
@@ -62,6 +102,7 @@ __global__ void __launch_bounds__(1024) prefill_recurrent_kernel(const RecParams
   float* sx = sC + R * N;         // [2][R][P]  x, by token parity
   float* red = sx + 2 * R * P;    // [G][R][P]
   float* sphi = red + G * R * P;  // [K]
+  float* sinv = sphi + K;         // [2R] BCNorm 1/RMS of the token's B, C rows (or prev_B)
 
   const Tin* xg = static_cast<const Tin*>(p.x);
   const Tin* Bg = static_cast<const Tin*>(p.B);
@@ -70,6 +111,18 @@ __global__ void __launch_bounds__(1024) prefill_recurrent_kernel(const RecParams
   const Tin* lamg = static_cast<const Tin*>(p.lam);
   const Tin* thg = static_cast<const Tin*>(p.theta);
   const float A = p.A[head];
+  const Tin* nwB = static_cast<const Tin*>(p.nwB);
+  const Tin* nbB = p.nbB ? static_cast<const Tin*>(p.nbB) + static_cast<size_t>(head) * N : nullptr;
+  const Tin* nwC = static_cast<const Tin*>(p.nwC);
+  const Tin* nbC = p.nbC ? static_cast<const Tin*>(p.nbC) + static_cast<size_t>(head) * N : nullptr;
+  // BCNorm and the bias of element n of a row scaled by 1/RMS `inv` (weights w, biases c)
+  auto nrm = [&](float v, float inv, const Tin* w, const Tin* c, int n) {
+    return fmaf(v * inv, w ? to_f(w[n]) : 1.f, c ? to_f(c[n]) : 0.f);
+  };
+  if (p.norm && p.prevB0) {
+    const Tin* pb0 = static_cast<const Tin*>(p.prevB0) + static_cast<size_t>(bh) * R * N;
+    rows_inv_rms<Tin>([&](int j) { return pb0 + static_cast<size_t>(j) * N; }, R, N, p.neps, sinv);
+  }
 
   // Entry state.  Slot 1 of the rotated-B / x buffers holds the previous token
   // (rotated by its own angle) because token 0 uses parity 0.
@@ -90,6 +143,10 @@ __global__ void __launch_bounds__(1024) prefill_recurrent_kernel(const RecParams
         const Tin* pb = static_cast<const Tin*>(p.prevB0) + (static_cast<size_t>(bh) * R + r) * N;
         u = to_f(pb[2 * k]);
         v = to_f(pb[2 * k + 1]);
+        if (p.norm) {  // the stored previous token is raw
+          u = nrm(u, sinv[r], nwB, nbB, 2 * k);
+          v = nrm(v, sinv[r], nwB, nbB, 2 * k + 1);
+        }
       }
       sB[(R + r) * N + 2 * k] = c * u + s * v;
       sB[(R + r) * N + 2 * k + 1] = -s * u + c * v;
@@ -107,6 +164,11 @@ __global__ void __launch_bounds__(1024) prefill_recurrent_kernel(const RecParams
     const float dt = to_f(dtg[tok]);
     const float lam = lamg ? to_f(lamg[tok]) : 1.f;  // no lambda, no theta: the Mamba-2 case
 
+    // 0. BCNorm: 1/RMS of the token's B and C rows (the barrier also ends the previous
+    //    token's reads of sinv)
+    if (p.norm)
+      rows_inv_rms<Tin>([&](int j) { return (j < R ? Bg : Cg) + (tok * R + (j % R)) * N; }, 2 * R,
+                        N, p.neps, sinv);
     // 1. advance the angle, rotate B_t and C_t; stage x_t.
     for (int k = threadIdx.x; k < K; k += blockDim.x) {
       const float ph = thg ? sphi[k] + dt * to_f(thg[tok * K + k]) : sphi[k];
@@ -115,8 +177,14 @@ __global__ void __launch_bounds__(1024) prefill_recurrent_kernel(const RecParams
       sincosf(ph, &s, &c);
       for (int r = 0; r < R; ++r) {
         const size_t o = (tok * R + r) * N + 2 * k;
-        const float bu = to_f(Bg[o]), bv = to_f(Bg[o + 1]);
-        const float cu = to_f(Cg[o]), cv = to_f(Cg[o + 1]);
+        float bu = to_f(Bg[o]), bv = to_f(Bg[o + 1]);
+        float cu = to_f(Cg[o]), cv = to_f(Cg[o + 1]);
+        if (p.norm) {
+          bu = nrm(bu, sinv[r], nwB, nbB, 2 * k);
+          bv = nrm(bv, sinv[r], nwB, nbB, 2 * k + 1);
+          cu = nrm(cu, sinv[R + r], nwC, nbC, 2 * k);
+          cv = nrm(cv, sinv[R + r], nwC, nbC, 2 * k + 1);
+        }
         sB[(cur * R + r) * N + 2 * k] = c * bu + s * bv;
         sB[(cur * R + r) * N + 2 * k + 1] = -s * bu + c * bv;
         sC[r * N + 2 * k] = c * cu + s * cv;
@@ -212,7 +280,7 @@ int plan_groups(const m3_dims& d) {
 }
 
 size_t rec_smem(const m3_dims& d, int G) {
-  return sizeof(float) * (3 * d.R * d.N + 2 * d.R * d.P + G * d.R * d.P + d.N / 2);
+  return sizeof(float) * (3 * d.R * d.N + 2 * d.R * d.P + G * d.R * d.P + d.N / 2 + 2 * d.R);
 }
 
 template <typename Tin, typename Tout>
@@ -222,7 +290,13 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
   RecParams p{a.x,      a.B,         a.C,         a.dt,        a.A,         a.lam,
               a.theta,  a.h0.h,      a.h0.phi,    a.h0.prev_B, a.h0.prev_x, a.y,
               a.hT.h,   a.hT.phi,    a.hT.prev_B, a.hT.prev_x, d.T,         d.H,
-              d.N,      d.P,         d.R,         G};
+              d.N,      d.P,         d.R,         G,
+              a.norm ? 1 : 0,
+              a.norm ? a.norm->B_weight : nullptr,
+              a.norm ? a.norm->B_bias : nullptr,
+              a.norm ? a.norm->C_weight : nullptr,
+              a.norm ? a.norm->C_bias : nullptr,
+              a.norm ? a.norm->eps : 1.f};
   const size_t smem = rec_smem(d, G);
   auto k = prefill_recurrent_kernel<Tin, Tout>;
   if (smem > 48 * 1024) {

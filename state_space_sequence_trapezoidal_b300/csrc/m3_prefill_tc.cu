@@ -120,6 +120,13 @@ struct TcParams {
   float* wsDphi;     // [B*H][nseg-1][N/2]   angle advanced over segment s
   const float* wsH;  // [B*H][nseg-1][N][P]  entry state of segment s + 1 (trapezoid term folded in)
   const float* wsPhi;  // [B*H][nseg-1][N/2] entry angle of segment s + 1
+  // BCNorm + biases of B and C (section 3.4), used when the kernel is built with kNorm:
+  // weights [N] (null: ones), biases [H][N] (null: zeros), epsilon.
+  const __nv_bfloat16* nwB;
+  const __nv_bfloat16* nbB;
+  const __nv_bfloat16* nwC;
+  const __nv_bfloat16* nbC;
+  float neps;
 };
 
 template <int NS, int R>
@@ -156,7 +163,8 @@ struct Cfg {
   static constexpr int M_HMAX = 1808;   // [2][4] per-warp max |h|
   static constexpr int M_CARRY = 1816;  // [2][64] angle carried into a chunk
   static constexpr int M_SCAN = 1944;   // [TB][K] angle partial sums
-  static constexpr int M_END = M_SCAN + TB * K;
+  static constexpr int M_NRM = M_SCAN + TB * K;  // [PG][4][8] bf16 BCNorm weights / biases
+  static constexpr int M_END = M_NRM + NS * 2;
   static constexpr uint32_t OFF_BAR = OFF_MISC + ((M_END * 4 + 15) / 16) * 16;
   static constexpr uint32_t OFF_HOLD = OFF_BAR + NUM_BARS * 8;  // TMEM base, abort flag
   static constexpr uint32_t SMEM_USED = OFF_HOLD + 16;
@@ -202,7 +210,11 @@ __device__ __forceinline__ float state_scale(float max_abs) {
 // exponential-Euler rule of Eq. (4), real transition; Remark 5's diagonal-only mask).  No
 // lambda or theta is read, B and C are only converted to fp16, and the caller passes no
 // angle or previous token.
-template <int NS, int R, bool kStateOnly, bool kRot>
+// kNorm: B and C arrive as raw projection outputs; BCNorm (RMS over the N entries of each
+// (token, rank) row, times a weight per state index) and the head's bias are applied by the
+// transform warps before the rotation (section 3.4), and to the stored previous token when
+// its trapezoid term is folded into the entry state.
+template <int NS, int R, bool kStateOnly, bool kRot, bool kNorm>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p) {
   using C = Cfg<NS, R>;
   constexpr int CT = C::CT, NB = C::NB, K = C::K, PG = C::PG, TB = C::TB, TPT = C::TPT;
@@ -452,6 +464,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     for (int u = 0; u < TPT; ++u) th_nxt[u] = make_uint2(0u, 0u);
     for (int k = xt; k < K; k += kXf)
       s_carry[k] = reduce_angle(phi0 ? phi0[k] : 0.f);
+    // BCNorm weights and this head's biases in shared memory, grouped by pair group: the
+    // 16-byte groups [8 pg, 8 pg + 8) of the B weight, B bias, C weight, C bias sit side by
+    // side, so a row's parameters are four 16-byte loads that the lanes of other token
+    // blocks share (bf16 1.0 is 0x3f80).  Published by the first transform barrier.
+    const uint4* s_nrm = reinterpret_cast<const uint4*>(misc + C::M_NRM);
+    if constexpr (kNorm) {
+      if (xt < 4 * PG) {
+        const int g = xt >> 2, which = xt & 3;
+        const __nv_bfloat16* src = which == 0 ? p.nwB : which == 1 ? p.nbB : which == 2 ? p.nwC : p.nbC;
+        uint4 v = (which & 1) ? make_uint4(0u, 0u, 0u, 0u)
+                              : make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
+        if (src) v = *reinterpret_cast<const uint4*>(src + ((which & 1) ? static_cast<size_t>(head) * NS : 0) + 8 * g);
+        reinterpret_cast<uint4*>(misc + C::M_NRM)[xt] = v;
+      }
+    }
     float range = 0.f;  // largest |value| converted to fp16
     bool ab = false;
 
@@ -534,6 +561,60 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           }
         }
         ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_FULL + s), (k >> 1) & 1, s_abort));
+        if (kNorm && !ab) {
+          // BCNorm pass: each of the thread's (token, rank) rows of the raw B and C tiles is
+          // normalised in place (RMS over its N entries, which the PG consecutive lanes of
+          // this pair group share: partial sums of squares, then a butterfly over those
+          // lanes, so every lane holds the same bits), scaled by the weights, shifted by the
+          // head's biases and rewritten as fp16 for the rotation below.
+          uint8_t* stg = sm + s * C::STAGE;
+          const int nb = pg >> 3, c16 = pg & 7;
+#pragma unroll 1
+          for (int u = 0; u < TPT; ++u) {
+            const int i = tb * TPT + u;
+#pragma unroll
+            for (int r = rs; r < R; r += RS) {
+              const uint32_t off = nb * 16384u + sw128(i * R + r, c16);
+              uint4 vb = *reinterpret_cast<const uint4*>(stg + off);
+              uint4 vc = kStateOnly ? make_uint4(0u, 0u, 0u, 0u)
+                                    : *reinterpret_cast<const uint4*>(stg + C::TILE + off);
+              uint32_t* wb = reinterpret_cast<uint32_t*>(&vb);
+              uint32_t* wc = reinterpret_cast<uint32_t*>(&vc);
+              float ssb = 0.f, ssc = 0.f;
+#pragma unroll
+              for (int qq = 0; qq < 4; ++qq) {
+                const float2 bb = unpack_bf16x2(wb[qq]), cc = unpack_bf16x2(wc[qq]);
+                ssb = fmaf(bb.x, bb.x, fmaf(bb.y, bb.y, ssb));
+                ssc = fmaf(cc.x, cc.x, fmaf(cc.y, cc.y, ssc));
+              }
+#pragma unroll
+              for (int o = PG / 2; o > 0; o >>= 1) {
+                ssb += __shfl_xor_sync(0xffffffffu, ssb, o);
+                ssc += __shfl_xor_sync(0xffffffffu, ssc, o);
+              }
+              const float nsb = rsqrtf(fmaf(ssb, 1.f / NS, p.neps));
+              const float nsc = rsqrtf(fmaf(ssc, 1.f / NS, p.neps));
+              const uint4 nwb4 = s_nrm[4 * pg + 0], nbb4 = s_nrm[4 * pg + 1];
+              const uint4 nwc4 = s_nrm[4 * pg + 2], nbc4 = s_nrm[4 * pg + 3];
+#pragma unroll
+              for (int qq = 0; qq < 4; ++qq) {
+                const float2 bb = __ffma2_rn(
+                    make_float2(unpack_bf16x2(wb[qq]).x * nsb, unpack_bf16x2(wb[qq]).y * nsb),
+                    unpack_bf16x2(reinterpret_cast<const uint32_t*>(&nwb4)[qq]),
+                    unpack_bf16x2(reinterpret_cast<const uint32_t*>(&nbb4)[qq]));
+                const float2 cc = __ffma2_rn(
+                    make_float2(unpack_bf16x2(wc[qq]).x * nsc, unpack_bf16x2(wc[qq]).y * nsc),
+                    unpack_bf16x2(reinterpret_cast<const uint32_t*>(&nwc4)[qq]),
+                    unpack_bf16x2(reinterpret_cast<const uint32_t*>(&nbc4)[qq]));
+                range = fmaxf(range, fmaxf(fmaxf(fabsf(bb.x), fabsf(bb.y)), fmaxf(fabsf(cc.x), fabsf(cc.y))));
+                wb[qq] = pack_f16x2(bb.x, bb.y);
+                wc[qq] = pack_f16x2(cc.x, cc.y);
+              }
+              *reinterpret_cast<uint4*>(stg + off) = vb;
+              if (!kStateOnly) *reinterpret_cast<uint4*>(stg + C::TILE + off) = vc;
+            }
+          }
+        }
         if (!ab) {
           uint8_t* stg = sm + s * C::STAGE;
           const int nb = pg >> 3, c16 = pg & 7;
@@ -570,7 +651,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 uint32_t* wc = reinterpret_cast<uint32_t*>(&vc);
 #pragma unroll
                 for (int qq = 0; qq < 4; ++qq) {
-                  const float2 bb = unpack_bf16x2(wb[qq]), cc = unpack_bf16x2(wc[qq]);
+                  // with BCNorm the tile already holds the normalised rows in fp16
+                  const float2 bb = kNorm ? unpack_f16x2(wb[qq]) : unpack_bf16x2(wb[qq]);
+                  const float2 cc = kNorm ? unpack_f16x2(wc[qq]) : unpack_bf16x2(wc[qq]);
                   float b0 = bb.x, b1 = bb.y, c0 = cc.x, c1 = cc.y;
                   if constexpr (kRot) {
                     const float c = cs[uu][qq], sv = sn[uu][qq];
@@ -842,7 +925,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll
         for (int r = 0; r < R; ++r) {
           const __nv_bfloat16* pb = prevB0 + r * NS + 2 * kk;
-          const float u = __bfloat162float(pb[0]), v = __bfloat162float(pb[1]);
+          float u = __bfloat162float(pb[0]), v = __bfloat162float(pb[1]);
+          if constexpr (kNorm) {  // the stored previous token is raw: BCNorm and bias first
+            float ss = 0.f;
+            for (int n = 0; n < NS; ++n) {
+              const float t = __bfloat162float(prevB0[r * NS + n]);
+              ss = fmaf(t, t, ss);
+            }
+            const float sc = rsqrtf(fmaf(ss, 1.f / NS, p.neps));
+            const float w0 = p.nwB ? __bfloat162float(p.nwB[2 * kk]) : 1.f;
+            const float w1 = p.nwB ? __bfloat162float(p.nwB[2 * kk + 1]) : 1.f;
+            const float c0 = p.nbB ? __bfloat162float(p.nbB[head * NS + 2 * kk]) : 0.f;
+            const float c1 = p.nbB ? __bfloat162float(p.nbB[head * NS + 2 * kk + 1]) : 0.f;
+            u = fmaf(u * sc, w0, c0);
+            v = fmaf(v * sc, w1, c1);
+          }
           bt[r] = (i & 1) ? (-sn * u + cs * v) : (cs * u + sn * v);
         }
       }
@@ -942,6 +1039,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             tmem_ld32(tmem + TM_YIN + lane_off + 32u * half, a);
             tmem_ld32(tmem + TM_YOFF + lane_off + 32u * half, c);
             tmem_ld_wait();
+            if (half == 1) {  // both accumulators are in registers: GEMM3/GEMM2 may refill them
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar(B_YFREE));
+            }
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
               uint32_t w[4];
@@ -969,6 +1071,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             if (lane == 0) bulk_wait_group_read0();
             __syncwarp();
             tmem_ld_wait();
+            if (half == 1) {  // both accumulators are in registers: GEMM3/GEMM2 may refill them
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar(B_YFREE));
+            }
 #pragma unroll
             for (int g = 0; g < 8; ++g) {
               float v[4];
@@ -985,9 +1092,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             }
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_YFREE));
       }
       sig_cur = sig_next;
     }
@@ -1067,6 +1171,10 @@ struct ScanParams {
   const float* wsDphi;
   float* wsH;
   float* wsPhi;
+  int norm;  // BCNorm + bias of the stored previous token (weights null: ones; biases null: zeros)
+  const __nv_bfloat16* nwB;
+  const __nv_bfloat16* nbB;
+  float neps;
 };
 
 __global__ void __launch_bounds__(1024) segment_scan_kernel(const ScanParams p) {
@@ -1088,8 +1196,20 @@ __global__ void __launch_bounds__(1024) segment_scan_kernel(const ScanParams p) 
     float sn, cs;
     sincosf(phi, &sn, &cs);
     for (int r = 0; r < R; ++r) {
-      const float u = __bfloat162float(p.prevB0[(static_cast<size_t>(bh) * R + r) * N + n0]);
-      const float v = __bfloat162float(p.prevB0[(static_cast<size_t>(bh) * R + r) * N + n1]);
+      const __nv_bfloat16* row = p.prevB0 + (static_cast<size_t>(bh) * R + r) * N;
+      float u = __bfloat162float(row[n0]), v = __bfloat162float(row[n1]);
+      if (p.norm) {
+        float ss = 0.f;
+        for (int n = 0; n < N; ++n) {
+          const float t = __bfloat162float(row[n]);
+          ss = fmaf(t, t, ss);
+        }
+        const float sc = rsqrtf(fmaf(ss, 1.f / N, p.neps));
+        u = fmaf(u * sc, p.nwB ? __bfloat162float(p.nwB[n0]) : 1.f,
+                 p.nbB ? __bfloat162float(p.nbB[head * N + n0]) : 0.f);
+        v = fmaf(v * sc, p.nwB ? __bfloat162float(p.nwB[n1]) : 1.f,
+                 p.nbB ? __bfloat162float(p.nbB[head * N + n1]) : 0.f);
+      }
       const float b0 = cs * u + sn * v, b1 = -sn * u + cs * v;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -1119,7 +1239,7 @@ __global__ void __launch_bounds__(1024) segment_scan_kernel(const ScanParams p) 
   }
 }
 
-template <int NS, int R, bool kRot>
+template <int NS, int R, bool kRot, bool kNorm>
 cudaError_t launch_nr(const PrefillArgs& a, cudaStream_t s) {
   using C = Cfg<NS, R>;
   const m3_dims& d = a.d;
@@ -1160,21 +1280,26 @@ cudaError_t launch_nr(const PrefillArgs& a, cudaStream_t s) {
   p.wsD = reinterpret_cast<float*>(a.ws + sg.off_d);
   p.wsDphi = reinterpret_cast<float*>(a.ws + sg.off_dphi);
   p.wsPhi = reinterpret_cast<float*>(a.ws + sg.off_phi);
+  p.nwB = kNorm ? static_cast<const __nv_bfloat16*>(a.norm->B_weight) : nullptr;
+  p.nbB = kNorm ? static_cast<const __nv_bfloat16*>(a.norm->B_bias) : nullptr;
+  p.nwC = kNorm ? static_cast<const __nv_bfloat16*>(a.norm->C_weight) : nullptr;
+  p.nbC = kNorm ? static_cast<const __nv_bfloat16*>(a.norm->C_bias) : nullptr;
+  p.neps = kNorm ? a.norm->eps : 1.f;
   const unsigned bhn = static_cast<unsigned>(d.B) * static_cast<unsigned>(d.H);
   cudaError_t e;
   if (sg.nseg > 1) {
-    auto k1 = prefill_tc_kernel<NS, R, true, kRot>;
+    auto k1 = prefill_tc_kernel<NS, R, true, kRot, kNorm>;
     e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     k1<<<bhn * static_cast<unsigned>(sg.nseg - 1), kThreads, C::SMEM_ALLOC, s>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     ScanParams q{NS, R, d.T, d.H, sg.nseg, p.h0, p.phi0, p.prevB0, p.prevx0, p.dt, p.lam,
                  p.wsU, p.wsD, p.wsDphi, p.wsU == nullptr ? nullptr : reinterpret_cast<float*>(a.ws + sg.off_h),
-                 reinterpret_cast<float*>(a.ws + sg.off_phi)};
+                 reinterpret_cast<float*>(a.ws + sg.off_phi), kNorm ? 1 : 0, p.nwB, p.nbB, p.neps};
     segment_scan_kernel<<<bhn, (NS / 2) * (kP / 4), 0, s>>>(q);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  auto k = prefill_tc_kernel<NS, R, false, kRot>;
+  auto k = prefill_tc_kernel<NS, R, false, kRot, kNorm>;
   e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
   k<<<bhn * static_cast<unsigned>(sg.nseg), kThreads, C::SMEM_ALLOC, s>>>(p);
@@ -1237,13 +1362,15 @@ bool prefill_tc_supported(const m3_dims& d) {
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
   // No theta: the Mamba-2 special case (lambda 1, no rotation, no previous token), SISO.
   if (!a.theta) {
-    if (a.d.R != 1 || a.lam || a.h0.phi || a.h0.prev_B || a.h0.prev_x) return cudaErrorInvalidValue;
-    if (a.d.N == 128) return launch_nr<128, 1, false>(a, s);
-    if (a.d.N == 64) return launch_nr<64, 1, false>(a, s);
+    if (a.d.R != 1 || a.lam || a.h0.phi || a.h0.prev_B || a.h0.prev_x || a.norm)
+      return cudaErrorInvalidValue;
+    if (a.d.N == 128) return launch_nr<128, 1, false, false>(a, s);
+    if (a.d.N == 64) return launch_nr<64, 1, false, false>(a, s);
     return cudaErrorInvalidValue;
   }
-#define M3_NR(NN, RR) \
-  if (a.d.N == NN && a.d.R == RR) return launch_nr<NN, RR, true>(a, s);
+#define M3_NR(NN, RR)                                                     \
+  if (a.d.N == NN && a.d.R == RR)                                         \
+    return a.norm ? launch_nr<NN, RR, true, true>(a, s) : launch_nr<NN, RR, true, false>(a, s);
   M3_NR(128, 1)
   M3_NR(128, 2)
   M3_NR(128, 4)

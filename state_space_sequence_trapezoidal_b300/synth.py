@@ -95,3 +95,32 @@ def make_inputs(B: int, T: int, H: int, P: int, N: int, R: int, seed: int, dtype
 def decode_step_seed(base_seed: int, step: int) -> int:
     """Seed of the per-token inputs of decode step ``step`` (0-based)."""
     return base_seed + 100 + step
+
+
+def make_raw_bc(inp: dict, seed: int, dtype: str = "bf16") -> dict:
+    """Raw B, C projection outputs for the BCNorm entry points: the drawn B and C with every
+    (token, head, rank) row scaled by its own random factor exp(N(0, 1)) (so the normalisation
+    has work to do), rounded to the input dtype.  Returns a copy of ``inp`` with B, C replaced."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = dict(inp)
+    for k in ("B", "C"):
+        sc = np.exp(rng.standard_normal(inp[k].shape[:-1] + (1,), dtype=np.float32))
+        v = (inp[k] * sc).astype(np.float32)
+        out[k] = round_bf16(v) if dtype == "bf16" else v
+    return out
+
+
+def make_bcnorm_params(N: int, H: int, R: int, seed: int, dtype: str = "bf16") -> dict:
+    """BCNorm weights [N] ~ U(0.5, 1.5) / sqrt(N R) and biases [H, N] ~ N(0, 0.09 / (N R)) for B
+    and for C, so that the normalised B, C have about the scale of the drawn ones; rounded to
+    the input dtype.  eps = 1e-5."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    s = np.float32(1.0 / np.sqrt(N * R))
+    p = {"B_weight": rng.uniform(0.5, 1.5, N).astype(np.float32) * s,
+         "B_bias": (0.3 * rng.standard_normal((H, N))).astype(np.float32) * s,
+         "C_weight": rng.uniform(0.5, 1.5, N).astype(np.float32) * s,
+         "C_bias": (0.3 * rng.standard_normal((H, N))).astype(np.float32) * s}
+    if dtype == "bf16":
+        p = {k: round_bf16(v) for k, v in p.items()}
+    p["eps"] = 1e-5
+    return p

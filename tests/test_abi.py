@@ -89,6 +89,33 @@ def test_workspace_size():
     assert m3.m3_ssm_prefill_workspace(_dims(B=1, T=16384, H=32, in_dtype=0)) == 256
 
 
+def test_bcnorm_entry_points_reject_bad_arguments():
+    """The fused BCNorm calls: norm required, eps > 0 and finite, parameters 16-byte aligned."""
+    lib = m3.load()
+    from state_space_sequence_trapezoidal_b300 import M3BcNorm
+
+    def pre(d, norm, x=16):
+        return lib.m3_ssm_prefill_bcnorm(ctypes.byref(d), x, 16, 16, 16, 16, 16, 16,
+                                         ctypes.byref(norm) if norm else None, None, 16, None,
+                                         16, 256, None)
+
+    def dec(d, norm, x=16):
+        st = M3State(16, 16, 16, 16)
+        return lib.m3_ssm_decode_step_bcnorm(ctypes.byref(d), ctypes.byref(st), x, 16, 16, 16, 16,
+                                             16, 16, ctypes.byref(norm) if norm else None, 16, None)
+
+    good = M3BcNorm(16, 32, None, 48, 1e-5)
+    for call in (pre, dec):
+        assert call(_dims(), None) == ARG
+        assert call(_dims(), M3BcNorm(16, 16, 16, 16, 0.0)) == ARG
+        assert call(_dims(), M3BcNorm(16, 16, 16, 16, -1.0)) == ARG
+        assert call(_dims(), M3BcNorm(16, 16, 16, 16, float("inf"))) == ARG
+        assert call(_dims(), M3BcNorm(16, 24, 16, 16, 1e-5)) == ALIGN
+        assert call(_dims(N=7), good) == SHAPE
+        assert call(_dims(), good, x=None) == ARG
+        assert call(_dims(), good, x=8) == ALIGN
+
+
 def test_decode_rejects_bad_arguments():
     lib = m3.load()
     st = M3State(16, 16, 16, 16)
