@@ -36,9 +36,12 @@ struct DecodeParams {
   const void* theta;
   void* y;
   int H, N, P;
-  // BCNorm + biases (section 3.4) of B_t, C_t and the stored raw previous B, when norm != 0:
-  // weights [N] (null: ones), biases [H][N] (null: zeros), in the input dtype.
-  int norm;
+};
+
+// BCNorm + biases (section 3.4) of B_t, C_t and the stored raw previous B, used when the
+// kernel is built with kNorm: weights [N] (null: ones), biases [H][N] (null: zeros), in the
+// input dtype.
+struct DecodeNorm {
   const void* nwB;
   const void* nbB;
   const void* nwC;
@@ -116,8 +119,11 @@ struct DecodeOcc {
 
 // kRot = false: the Mamba-2 special case (lambda = 1, theta = 0, Eq. (4)): h' = alpha h +
 // dt B_t X_t^T, y = h'^T C_t.  No angle, lambda or previous token is read or written.
-template <typename Tin, typename Tout, int R, int VPT, int MAXT, bool kRot>
-__global__ void __launch_bounds__(MAXT, DecodeOcc<R, MAXT>::kMinBlocks) decode_step_kernel(const DecodeParams p) {
+// kNorm: B_t, C_t and the stored previous B are raw projection outputs; BCNorm (RMS over
+// the N entries of each rank column, times a weight per state index) and the head's bias
+// are applied before the rotation (section 3.4).
+template <typename Tin, typename Tout, int R, int VPT, int MAXT, bool kRot, bool kNorm>
+__global__ void __launch_bounds__(MAXT, DecodeOcc<R, MAXT>::kMinBlocks) decode_step_kernel(const DecodeParams p, const DecodeNorm q) {
   const int bh = blockIdx.x;
   const int head = bh % p.H;
   const int N = p.N, P = p.P, K = N >> 1;
@@ -140,7 +146,7 @@ __global__ void __launch_bounds__(MAXT, DecodeOcc<R, MAXT>::kMinBlocks) decode_s
   float* sxp = sx + R * P;       // [R][P] X_{t-1}
   float* red = sxp + R * P;      // [RG][R][P] partial outputs
   float* sphi = red + RG * R * P; // [K] advanced angle
-  float* sinv = sphi + K;         // [3R] BCNorm 1/RMS of B_t, C_t, prev_B rows
+  float* sinv = sphi + K;         // [3R] BCNorm 1/RMS of the B_t, C_t, prev_B columns
 
   const Tin* Bt = static_cast<const Tin*>(p.B);
   const Tin* Ct = static_cast<const Tin*>(p.C);
@@ -167,13 +173,9 @@ __global__ void __launch_bounds__(MAXT, DecodeOcc<R, MAXT>::kMinBlocks) decode_s
     }
     __syncthreads();
   }
-  const Tin* nwB = static_cast<const Tin*>(p.nwB);
-  const Tin* nbB = p.nbB ? static_cast<const Tin*>(p.nbB) + static_cast<size_t>(head) * N : nullptr;
-  const Tin* nwC = static_cast<const Tin*>(p.nwC);
-  const Tin* nbC = p.nbC ? static_cast<const Tin*>(p.nbC) + static_cast<size_t>(head) * N : nullptr;
-  if (kRot && p.norm)
+  if constexpr (kNorm)
     row_inv_rms<Tin>(Bt + static_cast<size_t>(bh) * R * N, Ct + static_cast<size_t>(bh) * R * N,
-                     prevB + static_cast<size_t>(bh) * R * N, R, N, p.neps, sinv);
+                     prevB + static_cast<size_t>(bh) * R * N, R, N, q.neps, sinv);
   for (int i = threadIdx.x; kRot && (i < R * K || i < R * P); i += blockDim.x) {
     const bool rot = i < R * K, cpy = i < R * P;
     const int r = rot ? i / K : 0, k = rot ? i - r * K : 0;
@@ -201,7 +203,11 @@ __global__ void __launch_bounds__(MAXT, DecodeOcc<R, MAXT>::kMinBlocks) decode_s
       __sincosf(fmaf(-6.283185307179586f, rintf(ph0 * 0.15915494309189535f), ph0), &s0, &c0);
       __sincosf(fmaf(-6.283185307179586f, rintf(ph1 * 0.15915494309189535f), ph1), &s1, &c1);
       float bu = to_f(bu_raw), bv = to_f(bv_raw);
-      if (p.norm) {  // BCNorm and bias before the rotation; prev_B is stored raw
+      if constexpr (kNorm) {  // BCNorm and bias before the rotation; prev_B is stored raw
+        const Tin* nwB = static_cast<const Tin*>(q.nwB);
+        const Tin* nwC = static_cast<const Tin*>(q.nwC);
+        const Tin* nbB = q.nbB ? static_cast<const Tin*>(q.nbB) + static_cast<size_t>(head) * N : nullptr;
+        const Tin* nbC = q.nbC ? static_cast<const Tin*>(q.nbC) + static_cast<size_t>(head) * N : nullptr;
         const int n0 = 2 * k, n1 = 2 * k + 1;
         const float wb0 = nwB ? to_f(nwB[n0]) : 1.f, wb1 = nwB ? to_f(nwB[n1]) : 1.f;
         const float bb0 = nbB ? to_f(nbB[n0]) : 0.f, bb1 = nbB ? to_f(nbB[n1]) : 0.f;
@@ -284,14 +290,14 @@ __global__ void __launch_bounds__(MAXT, DecodeOcc<R, MAXT>::kMinBlocks) decode_s
 
 size_t smem_bytes(const m3_dims& d, int RG);
 
-template <typename Tin, typename Tout, int R, bool kRot>
+template <typename Tin, typename Tout, int R, bool kRot, bool kNorm>
 cudaError_t launch_r(const DecodeArgs& a, cudaStream_t s, int threads, int vpt) {
   const m3_dims& d = a.d;
   DecodeParams p{a.s.h, a.s.phi, a.s.prev_B, a.s.prev_x, a.x, a.B, a.C, a.dt, a.A, a.lam, a.theta,
-                 a.y, d.H, d.N, d.P, a.norm ? 1 : 0,
-                 a.norm ? a.norm->B_weight : nullptr, a.norm ? a.norm->B_bias : nullptr,
-                 a.norm ? a.norm->C_weight : nullptr, a.norm ? a.norm->C_bias : nullptr,
-                 a.norm ? a.norm->eps : 1.f};
+                 a.y, d.H, d.N, d.P};
+  DecodeNorm q{a.norm ? a.norm->B_weight : nullptr, a.norm ? a.norm->B_bias : nullptr,
+               a.norm ? a.norm->C_weight : nullptr, a.norm ? a.norm->C_bias : nullptr,
+               a.norm ? a.norm->eps : 1.f};
   const int RG = threads / (d.P / 2);
   const size_t smem = smem_bytes(d, RG);
   const dim3 grid(static_cast<unsigned>(d.B) * static_cast<unsigned>(d.H));
@@ -300,24 +306,24 @@ cudaError_t launch_r(const DecodeArgs& a, cudaStream_t s, int threads, int vpt) 
       cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
     }
-    k<<<grid, threads, smem, s>>>(p);
+    k<<<grid, threads, smem, s>>>(p, q);
     return cudaGetLastError();
   };
   if (threads <= 256) {
     switch (vpt) {
-      case 1: return go(decode_step_kernel<Tin, Tout, R, 1, 256, kRot>);
-      case 2: return go(decode_step_kernel<Tin, Tout, R, 2, 256, kRot>);
-      case 4: return go(decode_step_kernel<Tin, Tout, R, 4, 256, kRot>);
-      case 8: return go(decode_step_kernel<Tin, Tout, R, 8, 256, kRot>);
-      case 16: return go(decode_step_kernel<Tin, Tout, R, 16, 256, kRot>);
-      case 32: return go(decode_step_kernel<Tin, Tout, R, 32, 256, kRot>);
+      case 1: return go(decode_step_kernel<Tin, Tout, R, 1, 256, kRot, kNorm>);
+      case 2: return go(decode_step_kernel<Tin, Tout, R, 2, 256, kRot, kNorm>);
+      case 4: return go(decode_step_kernel<Tin, Tout, R, 4, 256, kRot, kNorm>);
+      case 8: return go(decode_step_kernel<Tin, Tout, R, 8, 256, kRot, kNorm>);
+      case 16: return go(decode_step_kernel<Tin, Tout, R, 16, 256, kRot, kNorm>);
+      case 32: return go(decode_step_kernel<Tin, Tout, R, 32, 256, kRot, kNorm>);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (vpt) {
-    case 8: return go(decode_step_kernel<Tin, Tout, R, 8, 1024, kRot>);
-    case 16: return go(decode_step_kernel<Tin, Tout, R, 16, 1024, kRot>);
-    case 32: return go(decode_step_kernel<Tin, Tout, R, 32, 1024, kRot>);
+    case 8: return go(decode_step_kernel<Tin, Tout, R, 8, 1024, kRot, kNorm>);
+    case 16: return go(decode_step_kernel<Tin, Tout, R, 16, 1024, kRot, kNorm>);
+    case 32: return go(decode_step_kernel<Tin, Tout, R, 32, 1024, kRot, kNorm>);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -365,23 +371,30 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   if (!a.theta) {
     if (a.d.R != 1 || a.lam || a.s.phi || a.s.prev_B || a.s.prev_x || a.norm)
       return cudaErrorInvalidValue;
-    if (bf_in && bf_out) return launch_r<__nv_bfloat16, __nv_bfloat16, 1, false>(a, s, threads, vpt);
-    if (bf_in) return launch_r<__nv_bfloat16, float, 1, false>(a, s, threads, vpt);
-    if (bf_out) return launch_r<float, __nv_bfloat16, 1, false>(a, s, threads, vpt);
-    return launch_r<float, float, 1, false>(a, s, threads, vpt);
+    if (bf_in && bf_out) return launch_r<__nv_bfloat16, __nv_bfloat16, 1, false, false>(a, s, threads, vpt);
+    if (bf_in) return launch_r<__nv_bfloat16, float, 1, false, false>(a, s, threads, vpt);
+    if (bf_out) return launch_r<float, __nv_bfloat16, 1, false, false>(a, s, threads, vpt);
+    return launch_r<float, float, 1, false, false>(a, s, threads, vpt);
   }
-#define M3_R(RR)                                                                                        \
-  if (a.d.R == RR) {                                                                                    \
-    if (bf_in && bf_out) return launch_r<__nv_bfloat16, __nv_bfloat16, RR, true>(a, s, threads, vpt);  \
-    if (bf_in) return launch_r<__nv_bfloat16, float, RR, true>(a, s, threads, vpt);                    \
-    if (bf_out) return launch_r<float, __nv_bfloat16, RR, true>(a, s, threads, vpt);                   \
-    return launch_r<float, float, RR, true>(a, s, threads, vpt);                                        \
+#define M3_RN(RR, NORM)                                                                                 \
+  if (bf_in && bf_out) return launch_r<__nv_bfloat16, __nv_bfloat16, RR, true, NORM>(a, s, threads, vpt); \
+  if (bf_in) return launch_r<__nv_bfloat16, float, RR, true, NORM>(a, s, threads, vpt);                   \
+  if (bf_out) return launch_r<float, __nv_bfloat16, RR, true, NORM>(a, s, threads, vpt);                  \
+  return launch_r<float, float, RR, true, NORM>(a, s, threads, vpt);
+#define M3_R(RR)          \
+  if (a.d.R == RR) {      \
+    if (a.norm) {         \
+      M3_RN(RR, true)     \
+    } else {              \
+      M3_RN(RR, false)    \
+    }                     \
   }
   M3_R(1)
   M3_R(2)
   M3_R(4)
   M3_R(8)
 #undef M3_R
+#undef M3_RN
   return cudaErrorInvalidValue;
 }
 

@@ -71,22 +71,25 @@ constexpr float kTwoPi = 6.283185307179586f;
 constexpr float kInvTwoPi = 0.15915494309189535f;
 constexpr float kF16Max = 65504.f;
 
-// mbarriers
+// mbarriers.  [S]: one per load stage (chunk k uses stage k % kStages); [2]: one per chunk
+// parity (score buffers in TMEM, decay sums and weights in shared memory).
+constexpr int kMaxStages = 3;
 enum {
-  B_FULL = 0,     // [2] TMA tiles of B and C landed
-  B_FULLX = 2,    // [2] TMA tile of X landed
-  B_BCFREE = 4,   // [2] B~, C~ of a stage no longer read (commit after GEMM3)
-  B_XFREE = 6,    // [2] X of a stage and the score buffer free again (commit after GEMM2)
-  B_XF = 8,       // [2] transform finished a chunk (one arrival per transform warp)
-  B_SFULL = 10,   // [2] scores in TMEM (commit after GEMM1)
-  B_PFULL = 12,   // [2] masked scores written back (one arrival per epilogue warp)
-  B_UFULL = 14,   // state increment U in TMEM (commit after GEMM4)
-  B_STATE = 15,   // state advanced: U read, next fp16 state copy in shared memory
-  B_HFREE = 16,   // GEMM3 finished reading the fp16 state copy (commit)
-  B_YFULL = 17,   // GEMM2 finished: both output accumulators complete (commit)
-  B_YFREE = 18,   // epilogue read both output accumulators
-  B_MFREE = 19,   // [2] both epilogue groups done with a chunk's decay sums and weights
-  NUM_BARS = 21
+  B_FULL = 0,     // [S] TMA tiles of B and C landed
+  B_FULLX = 3,    // [S] TMA tile of X landed
+  B_BCFREE = 6,   // [S] B~, C~ of a stage no longer read (commit after GEMM3)
+  B_XFREE = 9,    // [S] X of a stage no longer read (commit after GEMM2)
+  B_SFREE = 12,   // [2] score buffer free again (commit after GEMM2)
+  B_XF = 14,      // [2] transform finished a chunk (one arrival per transform warp)
+  B_SFULL = 16,   // [2] scores in TMEM (commit after GEMM1)
+  B_PFULL = 18,   // [2] masked scores written back (one arrival per epilogue warp)
+  B_UFULL = 20,   // state increment U in TMEM (commit after GEMM4)
+  B_STATE = 21,   // state advanced: U read, next fp16 state copy in shared memory
+  B_HFREE = 22,   // GEMM3 finished reading the fp16 state copy (commit)
+  B_YFULL = 23,   // GEMM2 finished: both output accumulators complete (commit)
+  B_YFREE = 24,   // epilogue read both output accumulators
+  B_MFREE = 25,   // [2] both epilogue groups done with a chunk's decay sums and weights
+  NUM_BARS = 27
 };
 
 struct TcParams {
@@ -144,7 +147,10 @@ struct Cfg {
   // shared memory (bytes from a 1024-aligned base)
   static constexpr uint32_t TILE = NB * 16384;         // 128 rows x NS, bf16 or fp16
   static constexpr uint32_t STAGE = 2 * TILE + 16384;  // B~, C~, X
-  static constexpr uint32_t OFF_DX = 2 * STAGE;        // d X, fp16 [128 rows][64]
+  // Load stages: three where they fit (N = 64), so that the next tiles are in flight
+  // while two chunks are being worked on; two for N = 128.
+  static constexpr int ST = NS == 64 ? 3 : 2;
+  static constexpr uint32_t OFF_DX = ST * STAGE;       // d X, fp16 [128 rows][64]
   static constexpr uint32_t OFF_H = OFF_DX + 16384;    // state copy, fp16 [NS rows n][64 p]
   static constexpr uint32_t OFF_Y = OFF_H + NS * 128;   // [4 warps][32 rows][128 B] y staging
   static constexpr uint32_t OFF_MISC = OFF_Y + 4 * 4096;
@@ -174,6 +180,7 @@ struct Cfg {
   static_assert(TB * TPT == CT && TB * RS == TBX && R % RS == 0, "rotation split");
   static_assert(CT <= kXf, "one discretisation thread per token");
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory");
+  static_assert(ST <= kMaxStages, "load stages");
 };
 
 __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk16) {
@@ -286,30 +293,34 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   if (warp == kWarpTma) {
     // ================================================================ TMA producer
     if (lane == 0) {
-      int issued[2] = {-1, -1}, issuedx[2] = {-1, -1};
+      constexpr int S = C::ST;
+      int issued[S], issuedx[S];
+#pragma unroll
+      for (int q = 0; q < S; ++q) issued[q] = issuedx[q] = -1;
       for (int k = 0; k < nchunks; ++k) {
-        const int s = k & 1;
-        const uint32_t st = sbase + s * C::STAGE;
-        // B and C of chunk k once GEMM3 of chunk k - 2 has finished with this stage
-        if (k >= 2 && !mbar_wait_abortable(bar(B_BCFREE + s), ((k >> 1) - 1) & 1, s_abort)) break;
-        mbar_arrive_expect_tx(bar(B_FULL + s), (kStateOnly ? 1 : 2) * C::TILE);
+        const int q = k % S;
+        const uint32_t st = sbase + q * C::STAGE;
+        // B and C of chunk k once GEMM3 of chunk k - S has finished with this stage
+        if (k >= S && !mbar_wait_abortable(bar(B_BCFREE + q), ((k / S) - 1) & 1, s_abort)) break;
+        mbar_arrive_expect_tx(bar(B_FULL + q), (kStateOnly ? 1 : 2) * C::TILE);
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
-          tma_load_5d(st + nb * 16384, &p.tmB, bar(B_FULL + s), 64 * nb, 0, head, a0 + k * CT, b);
+          tma_load_5d(st + nb * 16384, &p.tmB, bar(B_FULL + q), 64 * nb, 0, head, a0 + k * CT, b);
           if (!kStateOnly)
-            tma_load_5d(st + C::TILE + nb * 16384, &p.tmC, bar(B_FULL + s), 64 * nb, 0, head, a0 + k * CT, b);
+            tma_load_5d(st + C::TILE + nb * 16384, &p.tmC, bar(B_FULL + q), 64 * nb, 0, head, a0 + k * CT, b);
         }
-        issued[s] = k;
-        // X of chunk k once GEMM2 of chunk k - 2 has finished with it
-        if (k >= 2 && !mbar_wait_abortable(bar(B_XFREE + s), ((k >> 1) - 1) & 1, s_abort)) break;
-        mbar_arrive_expect_tx(bar(B_FULLX + s), 16384);
-        tma_load_5d(st + 2 * C::TILE, &p.tmX, bar(B_FULLX + s), 0, 0, head, a0 + k * CT, b);
-        issuedx[s] = k;
+        issued[q] = k;
+        // X of chunk k once GEMM2 of chunk k - S has finished with it
+        if (k >= S && !mbar_wait_abortable(bar(B_XFREE + q), ((k / S) - 1) & 1, s_abort)) break;
+        mbar_arrive_expect_tx(bar(B_FULLX + q), 16384);
+        tma_load_5d(st + 2 * C::TILE, &p.tmX, bar(B_FULLX + q), 0, 0, head, a0 + k * CT, b);
+        issuedx[q] = k;
       }
       // no copy may still be in flight when the CTA exits
-      for (int s = 0; s < 2; ++s) {
-        if (issued[s] >= 0) mbar_wait(bar(B_FULL + s), (issued[s] >> 1) & 1);
-        if (issuedx[s] >= 0) mbar_wait(bar(B_FULLX + s), (issuedx[s] >> 1) & 1);
+#pragma unroll
+      for (int q = 0; q < S; ++q) {
+        if (issued[q] >= 0) mbar_wait(bar(B_FULL + q), (issued[q] / S) & 1);
+        if (issuedx[q] >= 0) mbar_wait(bar(B_FULLX + q), (issuedx[q] / S) & 1);
       }
     }
   } else if (warp == kWarpMma) {
@@ -324,8 +335,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       uint32_t last_par = 0;
       if constexpr (kStateOnly) {
         for (int k = 0; k < nchunks; ++k) {
-          const int s = k & 1;
-          const uint32_t sB = sbase + s * C::STAGE;
+          const int s = k & 1, q = k % C::ST;
+          const uint32_t sB = sbase + q * C::STAGE;
           if (!mbar_wait_abortable(bar(B_XF + s), (k >> 1) & 1, s_abort)) break;
           if (!mbar_wait_abortable(bar(B_STATE), k & 1, s_abort)) break;
           tc_fence_after();
@@ -336,20 +347,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                       I_U, ks > 0);
           }
           tc_commit(bar(B_UFULL));
-          tc_commit(bar(B_BCFREE + s));
-          tc_commit(bar(B_XFREE + s));
-          last_bar = B_XFREE + s;
-          last_par = (k >> 1) & 1;
+          tc_commit(bar(B_BCFREE + q));
+          tc_commit(bar(B_XFREE + q));
+          last_bar = B_XFREE + q;
+          last_par = (k / C::ST) & 1;
         }
       }
       for (int k = 0; k < (kStateOnly ? 0 : nchunks); ++k) {
-        const int s = k & 1;
-        const uint32_t st = sbase + s * C::STAGE;
+        const int s = k & 1, q = k % C::ST;
+        const uint32_t st = sbase + q * C::STAGE;
         const uint32_t sB = st, sC = st + C::TILE, sX = st + 2 * C::TILE;
         const uint32_t tS = tmem + TM_S + 128u * s;
         if (!mbar_wait_abortable(bar(B_XF + s), (k >> 1) & 1, s_abort)) break;
         // the score buffer of this parity is free once GEMM2 of chunk k - 2 has read it
-        if (k >= 2 && !mbar_wait_abortable(bar(B_XFREE + s), ((k >> 1) - 1) & 1, s_abort)) break;
+        if (k >= 2 && !mbar_wait_abortable(bar(B_SFREE + s), ((k >> 1) - 1) & 1, s_abort)) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
@@ -379,9 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                     sdesc_sw128(sH + ks * 2048u, NS * 128u, 1024), I_CH, ks > 0);
         }
         tc_commit(bar(B_HFREE));
-        tc_commit(bar(B_BCFREE + s));
-        last_bar = B_BCFREE + s;
-        last_par = (k >> 1) & 1;
+        tc_commit(bar(B_BCFREE + q));
+        last_bar = B_BCFREE + q;
+        last_par = (k / C::ST) & 1;
         if (!mbar_wait_abortable(bar(B_PFULL + s), (k >> 1) & 1, s_abort)) break;
         tc_fence_after();
         // masked scores as A from TMEM: per 32-column block, 16 columns of bf16 hi pairs
@@ -397,8 +408,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                         sdesc_sw128(sX + j0 * 128u, 16384, 1024), I_PX, (blk | part | sub) != 0);
             }
         tc_commit(bar(B_YFULL));
-        tc_commit(bar(B_XFREE + s));
-        last_bar = B_XFREE + s;
+        tc_commit(bar(B_XFREE + q));
+        tc_commit(bar(B_SFREE + s));
+        last_bar = B_SFREE + s;
         last_par = (k >> 1) & 1;
       }
       // every MMA must be complete before the TMEM is released (the last commit tracks all)
@@ -560,14 +572,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             a3 += v.w;
           }
         }
-        ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_FULL + s), (k >> 1) & 1, s_abort));
+        const int q = k % C::ST;  // load stage of this chunk
+        ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_FULL + q), (k / C::ST) & 1, s_abort));
         if (kNorm && !ab) {
           // BCNorm pass: each of the thread's (token, rank) rows of the raw B and C tiles is
           // normalised in place (RMS over its N entries, which the PG consecutive lanes of
           // this pair group share: partial sums of squares, then a butterfly over those
           // lanes, so every lane holds the same bits), scaled by the weights, shifted by the
           // head's biases and rewritten as fp16 for the rotation below.
-          uint8_t* stg = sm + s * C::STAGE;
+          uint8_t* stg = sm + q * C::STAGE;
           const int nb = pg >> 3, c16 = pg & 7;
 #pragma unroll 1
           for (int u = 0; u < TPT; ++u) {
@@ -616,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           }
         }
         if (!ab) {
-          uint8_t* stg = sm + s * C::STAGE;
+          uint8_t* stg = sm + q * C::STAGE;
           const int nb = pg >> 3, c16 = pg & 7;
           // Tokens in groups of up to four: angles and sin/cos of the whole group first,
           // then the rows, so that independent work sits between dependent steps.
@@ -678,9 +691,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         }
         // d X into the single fp16 buffer, once GEMM4 of the previous chunk has read it
         if (k >= 1) ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_UFULL), (k - 1) & 1, s_abort));
-        ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_FULLX + s), (k >> 1) & 1, s_abort));
+        ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_FULLX + q), (k / C::ST) & 1, s_abort));
         if (!ab) {
-          const uint8_t* sx = sm + s * C::STAGE + 2 * C::TILE;
+          const uint8_t* sx = sm + q * C::STAGE + 2 * C::TILE;
           uint8_t* sdx = sm + C::OFF_DX;
           const int row = xt >> 1;
           const float dv = s_d[row >> C::kLogR];
