@@ -96,7 +96,6 @@ struct TcParams {
   CUtensorMap tmB;  // B [B][T][H][R][N] bf16, box {64, R, 1, CT, 1}
   CUtensorMap tmC;  // C, same
   CUtensorMap tmX;  // x [B][T][H][R][P] bf16, box {64, R, 1, CT, 1}
-  CUtensorMap tmY;  // y [B][T][H][R][P] fp32 (box {32, R, 1, 32/R, 1}) or bf16 (box {64, ...})
   const __nv_bfloat16* x;
   const __nv_bfloat16* B;
   const __nv_bfloat16* dt;
@@ -151,9 +150,9 @@ struct Cfg {
   // while two chunks are being worked on; two for N = 128.
   static constexpr int ST = NS == 64 ? 3 : 2;
   static constexpr uint32_t OFF_DX = ST * STAGE;       // d X, fp16 [128 rows][64]
-  static constexpr uint32_t OFF_H = OFF_DX + 16384;    // state copy, fp16 [NS rows n][64 p]
-  static constexpr uint32_t OFF_Y = OFF_H + NS * 128;   // [4 warps][32 rows][128 B] y staging
-  static constexpr uint32_t OFF_MISC = OFF_Y + 4 * 4096;
+  static constexpr uint32_t OFF_H = OFF_DX + 16384;    // state copy, fp16 [NS rows n][64 p]: high part
+  static constexpr uint32_t OFF_HL = OFF_H + NS * 128;  // and the fp16 rounding remainder (low part)
+  static constexpr uint32_t OFF_MISC = OFF_HL + NS * 128;
   // misc floats
   static constexpr int M_ELL = 0;       // [2][128] decay log2-sums
   static constexpr int M_W = 256;       // [2][128] trapezoid column weights
@@ -279,7 +278,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     tma_prefetch_desc(&p.tmB);
     tma_prefetch_desc(&p.tmC);
     tma_prefetch_desc(&p.tmX);
-    tma_prefetch_desc(&p.tmY);
   }
   if (warp == kWarpMma) {
     tmem_alloc(smem_u32(s_tmem), kTmemCols);
@@ -330,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       constexpr uint32_t I_CH = idesc_f16(128, 64, 0, 1);   // Y_off = C~ H  (H row-major)
       constexpr uint32_t I_U = idesc_f16(128, 64, 1, 1);    // U = B~^T (d X)
       constexpr uint32_t I_PX = idesc_bf16(128, 64, 0, 1);  // Y_in = P X
-      const uint32_t sDX = sbase + C::OFF_DX, sH = sbase + C::OFF_H;
+      const uint32_t sDX = sbase + C::OFF_DX, sH = sbase + C::OFF_H, sHl = sbase + C::OFF_HL;
       int last_bar = -1;
       uint32_t last_par = 0;
       if constexpr (kStateOnly) {
@@ -383,11 +381,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         last_par = k & 1;
         if (k >= 1 && !mbar_wait_abortable(bar(B_YFREE), (k - 1) & 1, s_abort)) break;
         tc_fence_after();
+        // C~ (H_hi + H_lo): the state copy in two fp16 parts keeps about 22 significant bits,
+        // so outputs dominated by a large state carry no more than the rounding of C~.
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
           const uint32_t ka = (ks >> 2) * 16384u + (ks & 3) * 32u;
           tc_mma_ss(tmem + TM_YOFF, sdesc_sw128(sC + ka, 16, 1024),
                     sdesc_sw128(sH + ks * 2048u, NS * 128u, 1024), I_CH, ks > 0);
+        }
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const uint32_t ka = (ks >> 2) * 16384u + (ks & 3) * 32u;
+          tc_mma_ss(tmem + TM_YOFF, sdesc_sw128(sC + ka, 16, 1024),
+                    sdesc_sw128(sHl + ks * 2048u, NS * 128u, 1024), I_CH, 1);
         }
         tc_commit(bar(B_HFREE));
         tc_commit(bar(B_BCFREE + q));
@@ -830,12 +836,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const float* s_elast = misc + C::M_ELAST;
     float* s_hmax = misc + C::M_HMAX;
     uint8_t* sHb = sm + C::OFF_H;
+    uint8_t* sHl = sm + C::OFF_HL;
     const size_t seq0 = (static_cast<size_t>(b) * Tg + a0) * H + head;  // token 0 of this segment
     const uint32_t tH = tmem + TM_H + lane_off;
-    uint8_t* sYw = sm + C::OFF_Y + ew * 4096;  // this warp's y staging rows
-    const uint32_t sYs = sbase + C::OFF_Y + ew * 4096;
 
     // fp16 copy of state row i (scaled by sig) as row i of the MN-major B operand of GEMM3
+    // fp16 copy of state row i (scaled by sig) as row i of the MN-major B operand of GEMM3,
+    // in two parts: hi = fp16(sig h) and lo = fp16(sig h - hi)
     auto put_state_row = [&](float sig) {
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
@@ -844,12 +851,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         tmem_ld_wait();
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-          uint4 w;
-          w.x = pack_f16x2(sig * __uint_as_float(hv[8 * g + 0]), sig * __uint_as_float(hv[8 * g + 1]));
-          w.y = pack_f16x2(sig * __uint_as_float(hv[8 * g + 2]), sig * __uint_as_float(hv[8 * g + 3]));
-          w.z = pack_f16x2(sig * __uint_as_float(hv[8 * g + 4]), sig * __uint_as_float(hv[8 * g + 5]));
-          w.w = pack_f16x2(sig * __uint_as_float(hv[8 * g + 6]), sig * __uint_as_float(hv[8 * g + 7]));
-          *reinterpret_cast<uint4*>(sHb + sw128(i, 4 * half + g)) = w;
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float v0 = sig * __uint_as_float(hv[8 * g + 2 * e]);
+            const float v1 = sig * __uint_as_float(hv[8 * g + 2 * e + 1]);
+            hi[e] = pack_f16x2(v0, v1);
+            const float2 hf = unpack_f16x2(hi[e]);
+            lo[e] = pack_f16x2(v0 - hf.x, v1 - hf.y);
+          }
+          *reinterpret_cast<uint4*>(sHb + sw128(i, 4 * half + g)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(sHl + sw128(i, 4 * half + g)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
     };
@@ -1036,27 +1048,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_STATE));
       // ---------------------------------------------------------- y = P X + e^{l} C~ H
-      // Each warp stages its 32 rows (128-byte swizzled) and one lane stores them with a
-      // TMA tensor store; rows past the end of the sequence are clipped by the store.
+      // Each thread writes its own row (one token and rank, P contiguous outputs) straight
+      // from registers; rows past the end of the sequence are not written.
       ab = ab || !__all_sync(0xffffffffu, mbar_wait_abortable(bar(B_YFULL), k & 1, s_abort));
       if (!ab) {
         tc_fence_after();
         const float f = el_i / sig_cur;
-        const int ty = a0 + t0 + (q * 32) / R;  // first token of this warp's rows
-        if (p.out_bf16) {
-          if (lane == 0) bulk_wait_group_read0();
-          __syncwarp();
+        const int tok = a0 + t0 + ti;  // this row's token
+        const bool row_ok = tok < Tg;
+        const size_t yo = ((static_cast<size_t>(b) * Tg + (row_ok ? tok : 0)) * H + head) * R * kP +
+                          static_cast<size_t>(i & (R - 1)) * kP;
 #pragma unroll 1
-          for (int half = 0; half < 2; ++half) {
-            uint32_t a[32], c[32];
-            tmem_ld32(tmem + TM_YIN + lane_off + 32u * half, a);
-            tmem_ld32(tmem + TM_YOFF + lane_off + 32u * half, c);
-            tmem_ld_wait();
-            if (half == 1) {  // both accumulators are in registers: GEMM3/GEMM2 may refill them
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(bar(B_YFREE));
-            }
+        for (int half = 0; half < 2; ++half) {
+          uint32_t a[32], c[32];
+          tmem_ld32(tmem + TM_YIN + lane_off + 32u * half, a);
+          tmem_ld32(tmem + TM_YOFF + lane_off + 32u * half, c);
+          tmem_ld_wait();
+          if (half == 1) {  // both accumulators are in registers: GEMM3/GEMM2 may refill them
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_YFREE));
+          }
+          if (p.out_bf16) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) + yo + 32 * half);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
               uint32_t w[4];
@@ -1066,49 +1080,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 w[e] = pack_bf16x2(fmaf(f, __uint_as_float(c[j]), __uint_as_float(a[j])),
                                    fmaf(f, __uint_as_float(c[j + 1]), __uint_as_float(a[j + 1])));
               }
-              *reinterpret_cast<uint4*>(sYw + sw128(lane, 4 * half + g)) = make_uint4(w[0], w[1], w[2], w[3]);
+              if (row_ok) __stcs(dst + g, make_uint4(w[0], w[1], w[2], w[3]));
             }
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0 && ty < Tg) {  // a box wholly past the end stores nothing
-            tma_store_5d(&p.tmY, sYs, 0, 0, head, ty, b);
-            bulk_commit_group();
-          }
-        } else {
-#pragma unroll 1
-          for (int half = 0; half < 2; ++half) {
-            uint32_t a[32], c[32];
-            tmem_ld32(tmem + TM_YIN + lane_off + 32u * half, a);
-            tmem_ld32(tmem + TM_YOFF + lane_off + 32u * half, c);
-            if (lane == 0) bulk_wait_group_read0();
-            __syncwarp();
-            tmem_ld_wait();
-            if (half == 1) {  // both accumulators are in registers: GEMM3/GEMM2 may refill them
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(bar(B_YFREE));
-            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.y) + yo + 32 * half);
 #pragma unroll
             for (int g = 0; g < 8; ++g) {
               float v[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e)
                 v[e] = fmaf(f, __uint_as_float(c[4 * g + e]), __uint_as_float(a[4 * g + e]));
-              *reinterpret_cast<float4*>(sYw + sw128(lane, g)) = make_float4(v[0], v[1], v[2], v[3]);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0 && ty < Tg) {
-              tma_store_5d(&p.tmY, sYs, 32 * half, 0, head, ty, b);
-              bulk_commit_group();
+              if (row_ok) __stcs(dst + g, make_float4(v[0], v[1], v[2], v[3]));
             }
           }
         }
       }
       sig_cur = sig_next;
     }
-    if (lane == 0) bulk_wait_group0();  // every y store complete before the CTA exits
     // ---------------------------------------------------------------- exit state
     if (!ab && last_seg && p.hT && swarp) {
       float4* dst = reinterpret_cast<float4*>(p.hT + (static_cast<size_t>(bh) * NS + i) * kP);
@@ -1262,10 +1250,6 @@ cudaError_t launch_nr(const PrefillArgs& a, cudaStream_t s) {
       !make_map(&p.tmX, a.x, d.B, d.T, d.H, R, kP, C::CT))
     return cudaErrorInvalidValue;
   const bool ybf = d.out_dtype == M3_BF16;
-  if (!make_map(&p.tmY, a.y, d.B, d.T, d.H, R, kP, 32 / R, ybf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                ybf ? 64u : 32u))
-    return cudaErrorInvalidValue;
   p.x = static_cast<const __nv_bfloat16*>(a.x);
   p.B = static_cast<const __nv_bfloat16*>(a.B);
   p.dt = static_cast<const __nv_bfloat16*>(a.dt);

@@ -106,9 +106,9 @@ def test_segmented_long_sequence_prefill(N, R, T, fresh):
 @pytest.mark.parametrize("N,R,T", [(128, 1, 1500), (64, 4, 600)])
 def test_oversized_entry_state(N, R, T):
     """An entry state far larger than any state the recurrence produces (h ~ N(0, 1)): the
-    outputs it dominates are ~20x the sequence's RMS.  The tensor-core operands are fp16
-    (11 significant bits), so the error scales with each output's own magnitude; the bound
-    here is 2e-2 of the largest output, and the exit state still meets the RMS bound."""
+    outputs it dominates reach 50-90x the sequence's RMS.  The state-to-output product takes
+    the state copy in two fp16 parts (about 22 significant bits), so those outputs carry only
+    the rounding of the rotated C, and the whole sequence meets the RMS bound."""
     B, H, Pd = 1, 4, 64
     inp = synth.make_inputs(B, T, H, Pd, N, R, 4000 + N + R + T, "bf16")
     st0 = P.random_state(B, H, N, Pd, R, "bf16", 19)
@@ -116,7 +116,9 @@ def test_oversized_entry_state(N, R, T):
     sl = P.all_slices(B, H)
     yr, sr = P.run_oracle(inp, sl, st0)
     got = P.pick(y.cpu().numpy(), sl, True)
-    assert np.max(np.abs(got - yr)) <= 2e-2 * np.max(np.abs(yr))
+    assert np.max(np.abs(yr)) > 40 * np.sqrt(np.mean(yr * yr))  # the case is what it claims
+    e = P.rel_err(got, yr)
+    assert e <= P.TOL["bf16"], e
     P.check_state({k: P.pick(v, sl, False) for k, v in P.state_to_host(hT).items()}, sr, "bf16")
 
 
