@@ -621,17 +621,17 @@ def main():
         # The same shapes through m3_ssd_* (lambda = 1, theta = 0: no trapezoid term, no
         # rotation, state h alone), as in the paper's Mamba-2 versus Mamba-3 decode table.
         sx = {k: d[k][:, :, :, 0].contiguous() for k in ("x", "B", "C")}
-        ys = torch.empty(w.B, w.T, w.H, 1, w.P, dtype=torch.float32, device=dev)
+        ys = torch.empty(w.B, w.T, w.H, 1, w.P, dtype=torch.bfloat16, device=dev)
         hs = torch.zeros(w.B, w.H, w.N, w.P, dtype=torch.float32, device=dev)
 
         def fs():
             m3.m3_ssd_prefill(sx["x"], sx["B"], sx["C"], d["dt"], d["A"], None, y=ys, hT=hs,
-                              workspace=ws)
+                              workspace=ws, out_dtype=torch.bfloat16)
 
         for _ in range(3):
             fs()
         mss = D.max_over_ranks(timed(fs, 20), dev)
-        bs = ssd_prefill_bytes(w)
+        bs = ssd_prefill_bytes(w, out_bytes=2)
         wd = synth.WORKLOADS[SISO_DEC]
         seed = D.rank_seed(wd.seed, rank)
         nsteps = args.decode_steps
