@@ -61,7 +61,7 @@ cudaError_t launch_prefill_recurrent(const PrefillArgs& a, cudaStream_t s);
 bool decode_supported(const m3_dims& d);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
-// Backward pass of the prefill (CUDA cores, fp32; checkpointed adjoint recurrence).
+// Backward pass of the prefill (CUDA cores, fp32; the chunked masked form transposed).
 struct BackwardArgs {
   m3_dims d;
   const void* x;
@@ -85,8 +85,8 @@ struct BackwardArgs {
   uint8_t* ws;
 };
 struct BackwardWorkspace {
-  int nch, kp;              // checkpoints per sequence, padded angle count
-  size_t off_da, off_ck, bytes;
+  int c, nch;  // tokens per chunk, chunks per sequence
+  size_t off_da, off_da_chunk, off_phi, off_sphi, off_dh0, off_h, off_g, bytes;
 };
 BackwardWorkspace backward_workspace(const m3_dims& d);
 bool backward_supported(const m3_dims& d);

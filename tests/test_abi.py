@@ -176,10 +176,11 @@ def test_backward_rejects_bad_arguments():
     assert call(_dims(), dh0=40) == ALIGN
 
 
-def test_backward_workspace_holds_the_checkpoints():
+def test_backward_workspace_holds_the_chunk_states():
     lib = m3.load()
     d = _dims(B=8, T=4096, H=32, P=64, N=128)
     n = lib.m3_ssm_prefill_backward_workspace(ctypes.byref(d))
-    # one N x P state (plus angles) every 16 tokens per (batch row, head)
-    assert n >= 8 * 32 * (4096 // 16) * 128 * 64 * 4
+    # per (batch row, head) and chunk of 32 tokens: the folded entry state and the exit
+    # cotangent, N x P floats each
+    assert n >= 2 * 8 * 32 * (4096 // 32) * 128 * 64 * 4
     assert lib.m3_ssm_prefill_backward_workspace(ctypes.byref(_dims(N=256, P=64))) == 256

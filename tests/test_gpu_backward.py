@@ -4,8 +4,9 @@ oracle (oracle/grad.py, pinned by finite differences of the C oracle).
 Every gradient tensor -- dx, dB, dC, ddt, dlambda, dtheta, dA, dh0 -- is compared element by
 element: max|gpu - oracle| / rms(oracle) <= 1e-4.  The kernel computes in fp32 from the exact
 input values (bf16 inputs are upcast exactly), so the fp32 tolerance applies to both input
-dtypes.  Shapes span the kernel's thread layouts (1 to 16 row groups), its recompute lengths
-(16, 8, 4 and 2 tokens per checkpoint) and ragged last stretches.
+dtypes.  Shapes span the kernels' chunk lengths (32, 16 and 4 tokens; 8 to 64 (token, rank)
+rows), chunk boundaries inside and at the end of the sequence, ragged last chunks, a single
+token, and the entry-state fold.
 """
 import numpy as np
 import pytest
@@ -66,7 +67,8 @@ def check(g, ref, sl, H, full_batch):
 
 @pytest.mark.parametrize("N,Pd,R,T", [(16, 16, 1, 40), (8, 12, 2, 37), (32, 32, 4, 20),
                                       (128, 64, 1, 50), (64, 64, 4, 33), (128, 64, 8, 9),
-                                      (6, 4, 1, 1)])
+                                      (6, 4, 1, 1), (128, 64, 1, 130), (64, 64, 4, 70),
+                                      (128, 64, 2, 100), (16, 8, 1, 64)])
 @pytest.mark.parametrize("with_state", [False, True])
 def test_backward_f32_matches_gradient_oracle(N, Pd, R, T, with_state):
     B, H = 2, 2
