@@ -11,30 +11,45 @@
 // Its adjoint is the same masked form transposed.  With Gout the cotangent of the chunk's
 // last state and Gh_i = C~_i^T dY_i (+ Gout at the last token):
 //   dC~_i = exp(l_i) dY_i Hp^T + sum_s D[i, s] B~_s,          D[i, s] = Mh[i, s] dY_i X_s^T
-//   dB~_s = sum_i D[i, s]^T C~_i + Mh[last, s] X_s Gout^T
-//   dX_s  = sum_i Mh[i, s] (C~_i B~_s^T)^T dY_i + Mh[last, s] B~_s Gout
-//   dHp   = sum_i exp(l_i) Gh_i   (= the cotangent of the previous chunk's last state)
+//   dB~_s = sum_i D[i, s]^T C~_i + wx_s X_s Gout^T
+//   dX_s  = sum_i Mh[i, s] (C~_i B~_s^T)^T dY_i + wx_s B~_s Gout
+//   dHp   = exp(l_last) Gout + sum_i exp(l_i) C~_i^T dY_i
 //   dMh[i, s] = <C~_i B~_s^T, dY_i X_s^T> (+ <Gout, B~_s^T X_s> on the last row)
-// then the chain rule through l, w, gamma, q, the fold and the rotation (dB = R(phi) dB~,
-// d phi from the rotation's derivative, d theta_t = dt_t sum_{s>=t} d phi_s over the whole
-// sequence).  MIMO rank R: rows are (token, rank) pairs and every rank pair of two tokens
-// shares the tokens' mask entry.
+// where wx_s = Mh[last, s], plus q of the next chunk's first token for the last token (its
+// trapezoid term is folded into the next chunk's Hp).  Then the chain rule through l, w,
+// gamma, q, the fold and the rotation (dB = R(phi) dB~, d phi from the rotation's
+// derivative, d theta_t = dt_t sum_{s>=t} d phi_s over the whole sequence).  MIMO rank R:
+// rows are (token, rank) pairs and every rank pair of two tokens shares their mask entry.
 //
-// Three kernels:
-//   bwd_scan_kernel      one CTA per (batch row, head): the chunk-level forward scan
-//                        H_in(k+1) = exp(l_last) Hp(k) + sum_s Mh[last, s] B~_s^T X_s, storing
-//                        every Hp(k) and the angle before every chunk, then the reverse scan
-//                        G(k-1) = dHp(k) = exp(l_last) G(k) + sum_i exp(l_i) C~_i^T dY_i,
-//                        storing every chunk's Gout.
-//   bwd_chunk_kernel     one CTA per (batch row, head, chunk), all chunks in parallel: the
-//                        adjoint above, the mask and fold parameters, the rotation adjoint and
-//                        the chunk-local suffix sums of d phi.
-//   bwd_finalize_kernel  one CTA per (batch row, head): adds the d phi of later chunks to
-//                        d theta and d dt, and sums the per-(b, h) part of dA.
-// A fourth kernel sums dA over batch rows.  Every reduction has a fixed order, so results are
-// bit-identical from run to run.
+// Frames.  Every chunk works in its own frame: B~, C~ rotated by the angle accumulated from
+// the chunk's start (psi_t), not from the sequence's.  Since the rotations of one pair
+// commute, the absolute B~ is the local one turned by the angle phi_b before the chunk, and a
+// state Z (rows = state entries) reads Z_loc = R(-phi_b) Z in the chunk's frame; inner products
+// over the state entries are the same in either frame.  Going from chunk k to k + 1 turns a
+// state by the chunk's angle advance sigma_k = psi_last.  Only the entry state (angle phi_0)
+// and the exit cotangent (angle before the last chunk) meet absolute angles.
+//
+// Kernels, in launch order:
+//   bwd_local_kernel   one CTA per (batch row, head, chunk): the chunk's own contributions to
+//                      the next chunk's folded state, dH = sum_s wx_s B~_s^T X_s, and to the
+//                      previous chunk's exit cotangent, dG = sum_i exp(l_i) C~_i^T dY_i (both
+//                      local frame), exp(l_last) and sigma.
+//   bwd_scan_kernel    one thread per (batch row, head, state pair, column), forward (Hp) or
+//                      reverse (Gout) over the chunks: Hp(k+1) = R(-sigma_k)(exp(l_last) Hp(k)
+//                      + dH(k)), Gout(k-1) = R(sigma_{k-1})(exp(l_last) Gout(k) + dG(k)), each
+//                      written over its chunk's dH / dG.
+//   bwd_chunk_kernel   one CTA per (batch row, head, chunk): the adjoint above, the mask and
+//                      fold parameters, the rotation adjoint, chunk-local suffix sums of d phi.
+//   bwd_carry_kernel   one CTA per (batch row, head): suffix sums of d phi over chunks, the
+//                      per-(b, h) part of dA, the fold gradient of the sequence's first token.
+//   bwd_apply_kernel   one CTA per (batch row, head, chunk): adds the later chunks' d phi to
+//                      d theta and d dt, and the fold gradient of the chunk's first token.
+//   dA_reduce_kernel   sums dA over batch rows.
+// Every reduction has a fixed order, so results are bit-identical from run to run.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <cstdint>
 
 #include "m3_internal.h"
 
@@ -70,12 +85,14 @@ struct BwdParams {
   float* dlam;
   float* dtheta;
   float* dh0;
-  float* wsPhi;   // [BH][nch][K]   angle of the token before chunk k, reduced to [-pi, pi]
-  float* wsH;     // [BH][nch][N*P] folded entry state Hp(k)
-  float* wsG;     // [BH][nch][N*P] cotangent of the state after the last token of chunk k
-  float* wsDH0;   // [BH][N*P]      cotangent of Hp(0)
-  float* wsSphi;  // [BH][nch][K]   sum of d phi over the chunk's tokens
-  float* wsDa;    // [BH][nch]      sum over the chunk's tokens of d(dt A) * dt
+  float* wsH;     // [BH][nch][N*P]  dH(k), then Hp(k) (chunk k's frame)
+  float* wsG;     // [BH][nch][N*P]  dG(k), then Gout(k) (chunk k's frame)
+  float* wsSig;   // [BH][nch][K]    angle advance over chunk k, reduced to [-pi, pi]
+  float* wsDec;   // [BH][nch]       exp(l_last) of chunk k
+  float* wsDH0;   // [BH][N*P]       cotangent of Hp(0) in chunk 0's frame
+  float* wsSphi;  // [BH][nch][K]    sum of d phi over chunk k, then over the chunks after k
+  float* wsDa;    // [BH][nch]       sum over chunk k's tokens of d(dt A) * dt
+  float* wsDqf;   // [BH][nch]       d q of chunk k's first token through the fold
   float* dApart;  // [BH]
   int T, H, N, P, R, c, M, nch, K;
 };
@@ -84,58 +101,127 @@ __device__ __forceinline__ float wrap(float a) {
   return fmaf(-6.283185307179586f, rintf(a * 0.15915494309189535f), a);
 }
 
-// out(i, j, sum_k A(i, k) B(k, j)) for i < NI, j < NJ, with both operands in shared memory
-// addressed by strides, A(i, k) = a[i * ai + k * ak] and B(k, j) = b[k * bk + j * bj]; TI x TJ
-// outputs per thread, tiles dealt to the CTA's threads in order.  Reads past NI / NJ are
-// clamped to the last row / column and their results dropped.
-template <int TI, int TJ, typename FO>
-__device__ __forceinline__ void sgemm(int NI, int NJ, int NK, const float* __restrict__ a, int ai,
-                                      int ak, const float* __restrict__ b, int bk, int bj, FO out) {
-  const int nti = (NI + TI - 1) / TI, ntj = (NJ + TJ - 1) / TJ;
-  for (int tile = threadIdx.x; tile < nti * ntj; tile += blockDim.x) {
-    const int i0 = (tile / ntj) * TI, j0 = (tile % ntj) * TJ;
-    const float* ap[TI];
-    const float* bp[TJ];
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(
+                   __cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// n consecutive floats of shared memory into registers (n = 1, 2 or 4; p aligned to 4 n bytes)
+template <int n>
+__device__ __forceinline__ void ldv(const float* p, float* d) {
+  if constexpr (n == 4) {
+    const float4 q = *reinterpret_cast<const float4*>(p);
+    d[0] = q.x, d[1] = q.y, d[2] = q.z, d[3] = q.w;
+  } else if constexpr (n == 2) {
+    const float2 q = *reinterpret_cast<const float2*>(p);
+    d[0] = q.x, d[1] = q.y;
+  } else {
+    d[0] = p[0];
+  }
+}
+
+// Register-tiled product over the CTA's warps: out(i, j, sum_k A(i, k) B(k, j)) for i < NI,
+// j < NJ.  A(i, k) = a[i * lda + k] when kAK (k contiguous), else a[k * lda + i];
+// B(k, j) = b[j * ldb + k] when kBK, else b[k * ldb + j].  A warp computes a (4 TI) x (8 TJ)
+// tile; lane (gi, gj) = (lane / 8, lane % 8) owns TI of its rows and TJ of its columns.  Along
+// a k-contiguous operand the lane's indices are interleaved (gi + 4 u, gj + 8 v), so that the
+// 4 (8) rows one load instruction touches fall in distinct banks for row strides of 4 (mod 32)
+// words; along an index-contiguous operand they are TI (TJ) consecutive indices read as one
+// vector.  kV: NK and the row strides are multiples of 4, the operands 16-byte aligned and
+// NI % TI == NJ % TJ == 0, and k advances four at a time with 16-byte loads along k;
+// otherwise one k at a time with scalar loads and interleaved indices in both operands.
+// Reads past NI / NJ are clamped to valid rows / columns and their results dropped.  Warp
+// tiles continue the round-robin of the previous product through rr, so that products
+// issued back to back without a barrier share the warps evenly.
+template <int TI, int TJ, bool kAK, bool kBK, bool kV, typename FO>
+__device__ __forceinline__ void gemm(int& rr, int NI, int NJ, int NK, const float* __restrict__ a,
+                                     int lda, const float* __restrict__ b, int ldb, FO out) {
+  constexpr bool kBlkI = kV && !kAK, kBlkJ = kV && !kBK;
+  constexpr int WI = 4 * TI, WJ = 8 * TJ;
+  const int lane = threadIdx.x & 31, nw = static_cast<int>(blockDim.x >> 5);
+  const int gi = lane >> 3, gj = lane & 7;
+  const int nwj = (NJ + WJ - 1) / WJ, ntile = ((NI + WI - 1) / WI) * nwj;
+  int w = static_cast<int>(threadIdx.x >> 5) - rr % nw;
+  if (w < 0) w += nw;
+  rr += ntile;
+  for (int t = w; t < ntile; t += nw) {
+    const int wi = (t / nwj) * WI, wj = (t % nwj) * WJ;
+    int ri[TI], rc[TI], cj[TJ], cc[TJ];
+    const int bi = kBlkI ? min(wi + gi * TI, NI - TI) : 0;
+    const int bj = kBlkJ ? min(wj + gj * TJ, NJ - TJ) : 0;
 #pragma unroll
-    for (int u = 0; u < TI; ++u) ap[u] = a + min(i0 + u, NI - 1) * ai;
+    for (int u = 0; u < TI; ++u) {
+      ri[u] = kBlkI ? wi + gi * TI + u : wi + gi + 4 * u;
+      rc[u] = kBlkI ? bi + u : min(ri[u], NI - 1);
+    }
 #pragma unroll
-    for (int v = 0; v < TJ; ++v) bp[v] = b + min(j0 + v, NJ - 1) * bj;
+    for (int v = 0; v < TJ; ++v) {
+      cj[v] = kBlkJ ? wj + gj * TJ + v : wj + gj + 8 * v;
+      cc[v] = kBlkJ ? bj + v : min(cj[v], NJ - 1);
+    }
     float acc[TI][TJ];
 #pragma unroll
     for (int u = 0; u < TI; ++u)
 #pragma unroll
       for (int v = 0; v < TJ; ++v) acc[u][v] = 0.f;
-#pragma unroll 4
-    for (int k = 0; k < NK; ++k) {
-      float av[TI], bv[TJ];
+    if constexpr (kV) {
+#pragma unroll 2
+      for (int k0 = 0; k0 < NK; k0 += 4) {
+        float av[4][TI], bv[4][TJ];
+        if constexpr (kAK) {
 #pragma unroll
-      for (int u = 0; u < TI; ++u) av[u] = ap[u][k * ak];
+          for (int u = 0; u < TI; ++u) {
+            float q[4];
+            ldv<4>(a + rc[u] * lda + k0, q);
 #pragma unroll
-      for (int v = 0; v < TJ; ++v) bv[v] = bp[v][k * bk];
+            for (int kk = 0; kk < 4; ++kk) av[kk][u] = q[kk];
+          }
+        } else {
 #pragma unroll
-      for (int u = 0; u < TI; ++u)
+          for (int kk = 0; kk < 4; ++kk) ldv<TI>(a + (k0 + kk) * lda + bi, av[kk]);
+        }
+        if constexpr (kBK) {
 #pragma unroll
-        for (int v = 0; v < TJ; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
+          for (int v = 0; v < TJ; ++v) {
+            float q[4];
+            ldv<4>(b + cc[v] * ldb + k0, q);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) bv[kk][v] = q[kk];
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) ldv<TJ>(b + (k0 + kk) * ldb + bj, bv[kk]);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+          for (int u = 0; u < TI; ++u)
+#pragma unroll
+            for (int v = 0; v < TJ; ++v) acc[u][v] = fmaf(av[kk][u], bv[kk][v], acc[u][v]);
+      }
+    } else {
+#pragma unroll 2
+      for (int k = 0; k < NK; ++k) {
+        float av[TI], bv[TJ];
+#pragma unroll
+        for (int u = 0; u < TI; ++u) av[u] = kAK ? a[rc[u] * lda + k] : a[k * lda + rc[u]];
+#pragma unroll
+        for (int v = 0; v < TJ; ++v) bv[v] = kBK ? b[cc[v] * ldb + k] : b[k * ldb + cc[v]];
+#pragma unroll
+        for (int u = 0; u < TI; ++u)
+#pragma unroll
+          for (int v = 0; v < TJ; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
+      }
     }
 #pragma unroll
     for (int u = 0; u < TI; ++u)
 #pragma unroll
       for (int v = 0; v < TJ; ++v)
-        if (i0 + u < NI && j0 + v < NJ) out(i0 + u, j0 + v, acc[u][v]);
-  }
-}
-
-// dst(i) = src(i) for i < n, four loads in flight per thread before their stores.
-template <typename FS, typename FD>
-__device__ __forceinline__ void stage(int n, FS src, FD dst) {
-  const int nt = blockDim.x;
-  for (int base = threadIdx.x; base < n; base += 4 * nt) {
-    float v[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) v[u] = base + u * nt < n ? src(base + u * nt) : 0.f;
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if (base + u * nt < n) dst(base + u * nt, v[u]);
+        if (ri[u] < NI && cj[v] < NJ) out(ri[u], cj[v], acc[u][v]);
   }
 }
 
@@ -157,533 +243,653 @@ __device__ float block_sum(float v, float* scratch) {
   return r;
 }
 
-// Per-token coefficients of one chunk (tokens t < nt; entries up to c zeroed): dt, lambda,
-// the chunk-local log-decay sums l, exp(l), gamma and q.  Warp 0, one lane per token.
-template <typename Tin>
-__device__ void chunk_coefs(const BwdParams& p, const Tin* dtg, const Tin* lamg, size_t tok0,
-                            size_t tok_stride, int nt, float A, float* s_dt, float* s_lam,
-                            float* s_ell, float* s_el, float* s_gam, float* s_q) {
-  if (threadIdx.x < 32) {
-    const int t = threadIdx.x;
-    const bool ok = t < nt;
-    const float dt = ok ? to_f(dtg[tok0 + t * tok_stride]) : 0.f;
-    const float lam = ok ? to_f(lamg[tok0 + t * tok_stride]) : 0.f;
-    float ell = dt * A;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float v = __shfl_up_sync(0xffffffffu, ell, o);
-      if (t >= o) ell += v;
-    }
-    if (t < p.c) {
-      s_dt[t] = dt;
-      s_lam[t] = lam;
-      s_ell[t] = ell;
-      s_el[t] = ok ? expf(ell) : 0.f;
-      s_gam[t] = lam * dt;
-      s_q[t] = (1.f - lam) * dt;
-    }
-  }
-}
-
-// theta of the chunk's tokens into s_th[c][K] (zero past nt).
-template <typename Tin>
-__device__ __forceinline__ void stage_theta(const Tin* thg, size_t tok0, size_t tok_stride, int nt,
-                                            int c, int K, float* s_th) {
-  stage(c * K, [&](int e) {
-    const int t = e / K;
-    return t < nt ? to_f(thg[(tok0 + static_cast<size_t>(t) * tok_stride) * K + (e - t * K)]) : 0.f;
-  }, [&](int e, float v) { s_th[e] = v; });
-}
-
-// Angles of the chunk's tokens: phi_t = phi_before + sum_{u<=t} dt_u theta_u (theta staged in
-// s_th), as cos / sin [c][K] of the angle reduced to [-pi, pi]; returns through s_phi the
-// reduced angle of the chunk's last token.
-__device__ void chunk_angles(int nt, int K, const float* s_dt, const float* s_th, float* s_phi,
-                             float* s_cs, float* s_sn) {
-  for (int k = threadIdx.x; k < K; k += blockDim.x) {
-    float ph = s_phi[k];
-    for (int t = 0; t < nt; ++t) {
-      ph = wrap(fmaf(s_dt[t], s_th[t * K + k], ph));
-      float sn, cs;
-      __sincosf(ph, &sn, &cs);
-      s_cs[t * K + k] = cs;
-      s_sn[t * K + k] = sn;
-    }
-    s_phi[k] = ph;
-  }
-}
-
-// Rows (token t < nt, rank r) of a [T][H][R][N] operand of this (b, h), rotated by the tokens'
-// angles, into dst[M][ld]; rows of tokens >= nt are zero.
-template <typename Tin>
-__device__ void load_rotated(const Tin* src, size_t tok0, size_t tok_stride, int nt, int R,
-                             int N, int K, int M, const float* s_cs, const float* s_sn,
-                             float* dst, int ld) {
-  // raw rows first (several loads in flight per thread), then the rotation in place
-  stage(M * N, [&](int e) {
-    const int row = e / N, t = row / R;
-    return t < nt ? to_f(src[((tok0 + static_cast<size_t>(t) * tok_stride) * R + (row - t * R)) * N + (e - row * N)])
-                  : 0.f;
-  }, [&](int e, float v) { dst[(e / N) * ld + e % N] = v; });
-  __syncthreads();
-  for (int e = threadIdx.x; e < M * K; e += blockDim.x) {
-    const int row = e / K, k = e - row * K, t = row / R;
-    const float u = dst[row * ld + 2 * k], v = dst[row * ld + 2 * k + 1];
-    const float cs = t < nt ? s_cs[t * K + k] : 1.f, sn = t < nt ? s_sn[t * K + k] : 0.f;
-    dst[row * ld + 2 * k] = cs * u + sn * v;
-    dst[row * ld + 2 * k + 1] = -sn * u + cs * v;
-  }
-}
-
-// Rows of a [T][H][R][P] operand into dst[M][ld] (zero past nt tokens).
-template <typename T>
-__device__ void load_rows(const T* src, size_t tok0, size_t tok_stride, int nt, int R, int P, int M,
-                          float* dst, int ld) {
-  stage(M * P, [&](int e) {
-    const int row = e / P, t = row / R;
-    return t < nt ? to_f(src[((tok0 + static_cast<size_t>(t) * tok_stride) * R + (row - t * R)) * P + (e - row * P)])
-                  : 0.f;
-  }, [&](int e, float v) { dst[(e / P) * ld + e % P] = v; });
-}
-
 // ------------------------------------------------------------------ shared-memory plans
-struct ScanSmem {
-  int H, BC, XY, th, cs, sn, prevB, prevX, phi, dt, lam, ell, el, gam, q, rs, red, total;
-};
-__host__ __device__ inline ScanSmem scan_smem(int N, int P, int R, int c) {
-  const int K = N / 2, M = c * R;
-  ScanSmem s{};
+struct Carve {
   int o = 0;
-  auto take = [&](int n) {
+  __host__ __device__ int take(int n) {
     const int at = o;
     o += (n + 3) & ~3;
     return at;
-  };
-  s.H = take(N * (P + kPad));
-  s.BC = take(M * (N + kPad));
-  s.XY = take(M * (P + kPad));
-  s.th = take(c * K);
-  s.cs = take(c * K);
-  s.sn = take(c * K);
-  s.prevB = take(R * N);
-  s.prevX = take(R * P);
-  s.phi = take(K);
-  s.dt = take(kMaxTok);
-  s.lam = take(kMaxTok);
-  s.ell = take(kMaxTok);
-  s.el = take(kMaxTok);
-  s.gam = take(kMaxTok);
-  s.q = take(kMaxTok);
-  s.rs = take(kMaxTok);
-  s.red = take(kThreads);
-  s.total = o;
+  }
+};
+// floats of staging for M x len elements of sz bytes copied raw (none for fp32: copied in place)
+__host__ __device__ inline int raw_floats(int M, int len, int sz) {
+  return sz == 4 ? 0 : (M * len * sz + 3) / 4;
+}
+
+// Per-chunk inputs shared by the local and adjoint kernels.
+struct InSmem {
+  int Bt, Ct, X, dY;               // fp32 rows [M][N + kPad] / [M][P + kPad]
+  int rB, rC, rX, rY;              // raw staging of 16-bit inputs
+  int th, cs, sn;                  // theta as loaded, cos / sin of psi [c][K]
+  int dt, lam, ell, el, gam, q;    // per token (q: c + 1, the next chunk's first token last)
+  int wx, rowel;                   // per row
+};
+__host__ __device__ inline void carve_inputs(Carve& cv, InSmem& s, int N, int P, int R, int c, int szIn,
+                                             int szDy, int raw_at) {
+  const int K = N / 2, M = c * R;
+  s.Bt = cv.take(M * (N + kPad));
+  s.Ct = cv.take(M * (N + kPad));
+  s.X = cv.take(M * (P + kPad));
+  s.dY = cv.take(M * (P + kPad));
+  s.th = cv.take((c * K * szIn + 3) / 4);
+  s.cs = cv.take(c * K);
+  s.sn = cv.take(c * K);
+  s.dt = cv.take(c);
+  s.lam = cv.take(c);
+  s.ell = cv.take(c);
+  s.el = cv.take(c);
+  s.gam = cv.take(c);
+  s.q = cv.take(c + 1);
+  s.wx = cv.take(M);
+  s.rowel = cv.take(M);
+  // raw staging: at raw_at when given (an area free until the inputs are converted)
+  Carve rc;
+  rc.o = raw_at >= 0 ? raw_at : cv.o;
+  s.rB = rc.take(raw_floats(M, N, szIn));
+  s.rC = rc.take(raw_floats(M, N, szIn));
+  s.rX = rc.take(raw_floats(M, P, szIn));
+  s.rY = rc.take(raw_floats(M, P, szDy));
+  if (raw_at < 0) cv.o = rc.o;
+}
+__host__ __device__ inline int raw_total(int N, int P, int R, int c, int szIn, int szDy) {
+  const int M = c * R;
+  auto r4 = [](int n) { return (n + 3) & ~3; };
+  return r4(raw_floats(M, N, szIn)) * 2 + r4(raw_floats(M, P, szIn)) + r4(raw_floats(M, P, szDy));
+}
+
+struct LocalSmem {
+  InSmem in;
+  int total;
+};
+__host__ __device__ inline LocalSmem local_smem(int N, int P, int R, int c, int szIn, int szDy) {
+  LocalSmem s{};
+  Carve cv;
+  carve_inputs(cv, s.in, N, P, R, c, szIn, szDy, -1);
+  s.total = cv.o;
   return s;
 }
 
 struct ChunkSmem {
-  int Bt, Ct, X, dY, Hp, Go, S, E, W, dCt, dBt, dphi, dM, Mh, ex, rowel, wx, th, cs, sn, prevB,
-      prevX, phi, dt, lam, ell, el, gam, q, dexp, dgam, dq, dell, red, total;
+  InSmem in;
+  int Q, XG, W, Hp, Go, S, E, dphi, Mh, ex, dM, dexp, wdot, dell, dgam, dq, red, total;
 };
-__host__ __device__ inline ChunkSmem chunk_smem(int N, int P, int R, int c) {
+__host__ __device__ inline ChunkSmem chunk_smem(int N, int P, int R, int c, int szIn, int szDy) {
   const int K = N / 2, M = c * R;
   ChunkSmem s{};
-  int o = 0;
-  auto take = [&](int n) {
-    const int at = o;
-    o += (n + 3) & ~3;
-    return at;
-  };
-  s.Bt = take(M * (N + kPad));   // B~
-  s.Ct = take(M * (N + kPad));   // C~
-  s.X = take(M * (P + kPad));
-  s.dY = take(M * (P + kPad));
-  s.Hp = take(N * (P + kPad));   // Hp
-  s.Go = take(N * (P + kPad));   // Gout
-  s.S = take(M * (M + kPad));    // C~ B~^T, then Mh o S
-  s.E = take(M * (M + kPad));    // dY X^T, then Mh o E
-  s.W = take(M * (P + kPad));    // B~ Gout
-  s.dCt = take(M * (N + kPad));  // dY Hp^T, then dC~
-  // dB~ [M][N + kPad] takes Hp's place once Hp is no longer read, where it fits
-  s.dBt = N * (P + kPad) >= M * (N + kPad) ? s.Hp : take(M * (N + kPad));
-  s.dphi = take(c * K);          // d phi per (token, pair), then its chunk-local suffix sums
-  s.dM = take(kMaxTok * (kMaxTok + 1));
-  s.Mh = take(kMaxTok * (kMaxTok + 1));   // Mh per token pair
-  s.ex = take(kMaxTok * (kMaxTok + 1));   // exp(l_i - l_s) per token pair
-  s.rowel = take(kMaxRows);               // exp(l) of each row's token
-  s.wx = take(kMaxRows);                  // each row's weight on the exit-state terms
-  s.th = take(c * K);
-  s.cs = take(c * K);
-  s.sn = take(c * K);
-  s.prevB = take(R * N);
-  s.prevX = take(R * P);
-  s.phi = take(K);
-  s.dt = take(kMaxTok);
-  s.lam = take(kMaxTok);
-  s.ell = take(kMaxTok);
-  s.el = take(kMaxTok);
-  s.gam = take(kMaxTok);
-  s.q = take(kMaxTok + 1);
-  s.dexp = take(kMaxTok);
-  s.dgam = take(kMaxTok);
-  s.dq = take(kMaxTok);
-  s.dell = take(kMaxTok);
-  s.red = take(kThreads);
-  s.total = o;
+  Carve cv;
+  s.Q = cv.take(M * (N + kPad));   // dY Hp^T, then dC~
+  s.XG = cv.take(M * (N + kPad));  // X Gout^T, then dB~
+  // the raw inputs wait in Q and XG when they fit there (both are written after conversion)
+  const int raw = raw_total(N, P, R, c, szIn, szDy);
+  carve_inputs(cv, s.in, N, P, R, c, szIn, szDy, raw <= 2 * M * (N + kPad) ? s.Q : -1);
+  s.W = cv.take(M * (P + kPad));   // B~ Gout
+  s.Hp = cv.take(N * (P + kPad));
+  s.Go = cv.take(N * (P + kPad));
+  s.S = cv.take(M * (M + kPad));   // C~ B~^T, then Mh o S
+  s.E = cv.take(M * (M + kPad));   // dY X^T, then Mh o E
+  // d phi per (token, pair) takes Hp's place (Hp is last read by the state products)
+  s.dphi = c * K <= N * (P + kPad) ? s.Hp : cv.take(c * K);
+  s.Mh = cv.take(c * (c + 1));
+  s.ex = cv.take(c * (c + 1));
+  s.dM = cv.take(c * (c + 1));
+  s.dexp = cv.take(c);
+  s.wdot = cv.take(c);
+  s.dell = cv.take(c);
+  s.dgam = cv.take(c);
+  s.dq = cv.take(c);
+  s.red = cv.take(kThreads);
+  s.total = cv.o;
   return s;
 }
 
-// ------------------------------------------------------------------ chunk-level scans
-template <typename Tin, typename Tdy>
-__global__ void __launch_bounds__(kThreads) bwd_scan_kernel(const BwdParams p) {
-  extern __shared__ float sm[];
-  const int bh = blockIdx.x, b = bh / p.H, head = bh % p.H;
-  const int N = p.N, P = p.P, R = p.R, c = p.c, M = p.M, K = p.K, NP = N * P;
-  const ScanSmem L = scan_smem(N, P, R, c);
-  float* sH = sm + L.H;
-  float* sBC = sm + L.BC;
-  float* sXY = sm + L.XY;
-  float* s_th = sm + L.th;
-  float* s_cs = sm + L.cs;
-  float* s_sn = sm + L.sn;
-  float* s_pB = sm + L.prevB;
-  float* s_pX = sm + L.prevX;
-  float* s_phi = sm + L.phi;
-  float* s_dt = sm + L.dt;
-  float* s_lam = sm + L.lam;
-  float* s_ell = sm + L.ell;
-  float* s_el = sm + L.el;
-  float* s_gam = sm + L.gam;
-  float* s_q = sm + L.q;
-  float* s_rs = sm + L.rs;
-  const int ldN = N + kPad, ldP = P + kPad;
-  const size_t tok_stride = p.H;
-  const size_t seq0 = static_cast<size_t>(b) * p.T * p.H + head;
-  const Tin* Bg = static_cast<const Tin*>(p.B);
-  const Tin* Cg = static_cast<const Tin*>(p.C);
-  const Tin* xg = static_cast<const Tin*>(p.x);
-  const Tin* dtg = static_cast<const Tin*>(p.dt);
-  const Tin* lamg = static_cast<const Tin*>(p.lam);
-  const Tin* thg = static_cast<const Tin*>(p.theta);
-  const Tdy* dyg = static_cast<const Tdy*>(p.dy);
-  const float A = p.A[head];
+// ------------------------------------------------------------------ chunk inputs
+struct ChunkPos {
+  int k, t0, nt, last;
+  bool has_next;
+  size_t tok0;  // index of (b, t0, h) in [B][T][H]
+};
+__device__ __forceinline__ ChunkPos chunk_pos(const BwdParams& p, int bh, int k) {
+  ChunkPos q;
+  const int b = bh / p.H, head = bh % p.H;
+  q.k = k;
+  q.t0 = k * p.c;
+  q.nt = min(p.c, p.T - q.t0);
+  q.last = q.nt - 1;
+  q.has_next = k + 1 < p.nch;
+  q.tok0 = (static_cast<size_t>(b) * p.T + q.t0) * p.H + head;
+  return q;
+}
 
-  // entry state, angle and previous token (rotated by its own angle)
-  for (int e = threadIdx.x; e < NP; e += blockDim.x)
-    sH[(e / P) * ldP + e % P] = p.h0 ? p.h0[static_cast<size_t>(bh) * NP + e] : 0.f;
-  for (int k = threadIdx.x; k < K; k += blockDim.x) {
-    const float ph = p.phi0 ? wrap(p.phi0[static_cast<size_t>(bh) * K + k]) : 0.f;
-    s_phi[k] = ph;
+// Rows (token t < c, rank r) of a [T][H][R][len] operand of the chunk into dst[M][ld] as fp32,
+// rows of tokens >= nt zero.  kV: 16-byte asynchronous copies, straight into dst for fp32 or
+// into raw for 16-bit types (converted by finish_rows); else plain scalar loads.
+template <typename T, bool kV>
+__device__ void issue_rows(const T* src, const ChunkPos& q, size_t tok_stride, int c, int R, int len,
+                           float* dst, int ld, T* raw) {
+  if constexpr (kV) {
+    constexpr int vec = 16 / sizeof(T);
+    const int per_row = len / vec, n = c * R * per_row;
+    for (int e = threadIdx.x; e < n; e += blockDim.x) {
+      const int row = e / per_row, col = (e - row * per_row) * vec, t = row / R;
+      if (t < q.nt) {
+        const T* g = src + ((q.tok0 + static_cast<size_t>(t) * tok_stride) * R + (row - t * R)) * len + col;
+        if constexpr (sizeof(T) == 4)
+          cp_async16(dst + row * ld + col, g);
+        else
+          cp_async16(raw + row * len + col, g);
+      } else if constexpr (sizeof(T) == 4) {
+        *reinterpret_cast<float4*>(dst + row * ld + col) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+  } else {
+    const int n = c * R * len;
+    for (int base = threadIdx.x; base < n; base += 4 * blockDim.x) {
+      float v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = base + u * blockDim.x, row = e / len, t = row / R;
+        v[u] = e < n && t < q.nt
+                   ? to_f(src[((q.tok0 + static_cast<size_t>(t) * tok_stride) * R + (row - t * R)) * len + (e - row * len)])
+                   : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = base + u * blockDim.x, row = e / len;
+        if (e < n) dst[row * ld + (e - row * len)] = v[u];
+      }
+    }
+  }
+}
+
+// After the copies have landed: each row's values (raw 16-bit staging, or dst in place),
+// rotated pairwise by the token's psi when rot, times rowscale[row] when given, into dst.
+template <typename T, bool kV>
+__device__ void finish_rows(const ChunkPos& q, int c, int R, int len, float* dst, int ld, const T* raw,
+                            bool rot, const float* s_cs, const float* s_sn, int K, const float* rowscale) {
+  constexpr bool kRaw = kV && sizeof(T) != 4;
+  const int M = c * R;
+  if (rot) {
+    for (int e = threadIdx.x; e < M * K; e += blockDim.x) {
+      const int row = e / K, kk = e - row * K, t = row / R;
+      float o0 = 0.f, o1 = 0.f;  // rows past nt: zero (their raw staging was never written)
+      if (t < q.nt) {
+        float u, v;
+        if constexpr (kRaw) {
+          u = to_f(raw[row * len + 2 * kk]);
+          v = to_f(raw[row * len + 2 * kk + 1]);
+        } else {
+          u = dst[row * ld + 2 * kk];
+          v = dst[row * ld + 2 * kk + 1];
+        }
+        const float cs = s_cs[t * K + kk], sn = s_sn[t * K + kk];
+        const float sc = rowscale ? rowscale[row] : 1.f;
+        o0 = sc * fmaf(cs, u, sn * v);
+        o1 = sc * fmaf(cs, v, -sn * u);
+      }
+      dst[row * ld + 2 * kk] = o0;
+      dst[row * ld + 2 * kk + 1] = o1;
+    }
+  } else if (kRaw || rowscale) {
+    for (int e = threadIdx.x; e < M * len; e += blockDim.x) {
+      const int row = e / len, col = e - row * len, t = row / R;
+      float o = 0.f;
+      if (t < q.nt) {
+        const float u = kRaw ? to_f(raw[e]) : dst[row * ld + col];
+        o = rowscale ? rowscale[row] * u : u;
+      }
+      dst[row * ld + col] = o;
+    }
+  }
+}
+
+// Per-token coefficients (warp 0, one lane per token, tokens >= nt zero): dt, lambda, the
+// chunk-local log-decay sums l, exp(l), gamma, q, and q of the next chunk's first token.
+template <typename Tin>
+__device__ void chunk_coefs(const BwdParams& p, const ChunkPos& q, float A, const InSmem& L, float* sm) {
+  if (threadIdx.x < 32) {
+    const Tin* dtg = static_cast<const Tin*>(p.dt);
+    const Tin* lamg = static_cast<const Tin*>(p.lam);
+    const int t = threadIdx.x;
+    const bool ok = t < q.nt;
+    const size_t o = q.tok0 + static_cast<size_t>(t) * p.H;
+    const float dt = ok ? to_f(dtg[o]) : 0.f;
+    const float lam = ok ? to_f(lamg[o]) : 0.f;
+    float ell = dt * A;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const float v = __shfl_up_sync(0xffffffffu, ell, d);
+      if (t >= d) ell += v;
+    }
+    if (t < p.c) {
+      sm[L.dt + t] = dt;
+      sm[L.lam + t] = lam;
+      sm[L.ell + t] = ell;
+      sm[L.el + t] = ok ? expf(ell) : 0.f;
+      sm[L.gam + t] = lam * dt;
+      sm[L.q + t] = (1.f - lam) * dt;
+    }
+    if (t == 0) {
+      const size_t tn = q.tok0 + static_cast<size_t>(q.nt) * p.H;
+      sm[L.q + p.c] = q.has_next ? (1.f - to_f(lamg[tn])) * to_f(dtg[tn]) : 0.f;
+    }
+  }
+}
+
+// theta rows of the chunk into the th area (asynchronous copies when kV, else fp32 scalars).
+template <typename Tin, bool kV>
+__device__ void issue_theta(const BwdParams& p, const ChunkPos& q, float* s_th) {
+  const Tin* thg = static_cast<const Tin*>(p.theta);
+  const int K = p.K;
+  if constexpr (kV) {
+    constexpr int vec = 16 / sizeof(Tin);
+    const int per = K / vec, n = q.nt * per;
+    Tin* dst = reinterpret_cast<Tin*>(s_th);
+    for (int e = threadIdx.x; e < n; e += blockDim.x) {
+      const int t = e / per, col = (e - t * per) * vec;
+      cp_async16(dst + t * K + col, thg + (q.tok0 + static_cast<size_t>(t) * p.H) * K + col);
+    }
+  } else {
+    for (int e = threadIdx.x; e < q.nt * K; e += blockDim.x) {
+      const int t = e / K;
+      s_th[e] = to_f(thg[(q.tok0 + static_cast<size_t>(t) * p.H) * K + (e - t * K)]);
+    }
+  }
+}
+template <typename Tin, bool kV>
+__device__ __forceinline__ float theta_at(const float* s_th, int e) {
+  if constexpr (kV)
+    return to_f(reinterpret_cast<const Tin*>(s_th)[e]);
+  else
+    return s_th[e];
+}
+
+// psi_t = sum_{u <= t} dt_u theta_u from the chunk's start, reduced to [-pi, pi] at every
+// step, as cos / sin [c][K] (identity past nt); returns psi of the last token per pair.
+template <typename Tin, bool kV>
+__device__ void chunk_angles(const ChunkPos& q, int c, int K, const float* sm, const InSmem& L,
+                             float* s_cs, float* s_sn, float* sig_out) {
+  const float* s_th = sm + L.th;
+  for (int kk = threadIdx.x; kk < K; kk += blockDim.x) {
+    float ph = 0.f;
+    for (int t = 0; t < c; ++t) {
+      float sn = 0.f, cs = 1.f;
+      if (t < q.nt) {
+        ph = wrap(fmaf(sm[L.dt + t], theta_at<Tin, kV>(s_th, t * K + kk), ph));
+        __sincosf(ph, &sn, &cs);
+      }
+      s_cs[t * K + kk] = cs;
+      s_sn[t * K + kk] = sn;
+    }
+    if (sig_out) sig_out[kk] = ph;
+  }
+}
+
+// The chunk's inputs: coefficients, theta and psi, and B~, C~ (rotated by psi), X, dY as
+// fp32 rows, X rows times xscale and dY rows times yscale when given.  extra() issues further
+// asynchronous copies with the inputs' (it runs after theta's copies are committed); the
+// function returns with every copy landed and a barrier passed.
+template <typename Tin, typename Tdy, bool kV, typename FX, typename FS>
+__device__ void load_chunk(const BwdParams& p, const ChunkPos& q, float A, const InSmem& L, float* sm,
+                           float* sig_out, FX extra, FS scales, bool scale_x, bool scale_y) {
+  const int N = p.N, P = p.P, R = p.R, c = p.c, K = p.K;
+  const size_t ts = p.H;
+  issue_theta<Tin, kV>(p, q, sm + L.th);
+  if constexpr (kV) cp_async_commit();
+  issue_rows<Tin, kV>(static_cast<const Tin*>(p.B), q, ts, c, R, N, sm + L.Bt, N + kPad,
+                      reinterpret_cast<Tin*>(sm + L.rB));
+  issue_rows<Tin, kV>(static_cast<const Tin*>(p.C), q, ts, c, R, N, sm + L.Ct, N + kPad,
+                      reinterpret_cast<Tin*>(sm + L.rC));
+  issue_rows<Tin, kV>(static_cast<const Tin*>(p.x), q, ts, c, R, P, sm + L.X, P + kPad,
+                      reinterpret_cast<Tin*>(sm + L.rX));
+  issue_rows<Tdy, kV>(static_cast<const Tdy*>(p.dy), q, ts, c, R, P, sm + L.dY, P + kPad,
+                      reinterpret_cast<Tdy*>(sm + L.rY));
+  extra();
+  if constexpr (kV) cp_async_commit();
+  chunk_coefs<Tin>(p, q, A, L, sm);
+  if constexpr (kV) asm volatile("cp.async.wait_group 1;" ::: "memory");
+  __syncthreads();
+  chunk_angles<Tin, kV>(q, c, K, sm, L, sm + L.cs, sm + L.sn, sig_out);
+  scales();  // per-row weights from the coefficients
+  if constexpr (kV) cp_async_wait_all();
+  __syncthreads();
+  finish_rows<Tin, kV>(q, c, R, N, sm + L.Bt, N + kPad, reinterpret_cast<const Tin*>(sm + L.rB), true,
+                       sm + L.cs, sm + L.sn, K, nullptr);
+  finish_rows<Tin, kV>(q, c, R, N, sm + L.Ct, N + kPad, reinterpret_cast<const Tin*>(sm + L.rC), true,
+                       sm + L.cs, sm + L.sn, K, nullptr);
+  finish_rows<Tin, kV>(q, c, R, P, sm + L.X, P + kPad, reinterpret_cast<const Tin*>(sm + L.rX), false,
+                       nullptr, nullptr, K, scale_x ? sm + L.wx : nullptr);
+  finish_rows<Tdy, kV>(q, c, R, P, sm + L.dY, P + kPad, reinterpret_cast<const Tdy*>(sm + L.rY), false,
+                       nullptr, nullptr, K, scale_y ? sm + L.rowel : nullptr);
+  __syncthreads();
+}
+
+// Per row: wx, its weight on the exit-state terms (Mh[last, t], plus q of the next chunk's
+// first token for the last token, whose trapezoid term that chunk folds in), and exp(l) of
+// its token.  Needs the coefficients (a barrier after chunk_coefs).
+__device__ void row_weights(const ChunkPos& q, int c, int R, const InSmem& L, float* sm) {
+  for (int row = threadIdx.x; row < c * R; row += blockDim.x) {
+    const int t = row / R;
+    float wx = 0.f;
+    if (t < q.nt)
+      wx = t == q.last ? sm[L.gam + t] + sm[L.q + c]
+                       : expf(sm[L.ell + q.last] - sm[L.ell + t]) * (sm[L.gam + t] + sm[L.q + t + 1]);
+    sm[L.wx + row] = wx;
+    sm[L.rowel + row] = sm[L.el + t];
+  }
+}
+
+// ------------------------------------------------------------------ chunk-local state terms
+template <typename Tin, typename Tdy, bool kV>
+__global__ void __launch_bounds__(kThreads) bwd_local_kernel(const BwdParams p) {
+  extern __shared__ __align__(16) float sm[];
+  const int bh = blockIdx.x / p.nch, k = blockIdx.x % p.nch;
+  const ChunkPos q = chunk_pos(p, bh, k);
+  const int N = p.N, P = p.P, R = p.R, c = p.c, M = p.M, K = p.K;
+  const LocalSmem S = local_smem(N, P, R, c, sizeof(Tin), sizeof(Tdy));
+  const InSmem& L = S.in;
+  const size_t slot = static_cast<size_t>(bh) * p.nch + k;
+  load_chunk<Tin, Tdy, kV>(p, q, p.A[bh % p.H], L, sm, p.wsSig + slot * K, [] {},
+                           [&] { row_weights(q, c, R, L, sm); }, true, true);
+  if (threadIdx.x == 0) p.wsDec[slot] = sm[L.el + q.last];
+  // dH[n][p] = sum_s B~[s][n] (wx_s X[s][p]),  dG[n][p] = sum_i C~[i][n] (exp(l_i) dY[i][p])
+  float* dH = p.wsH + slot * N * P;
+  float* dG = p.wsG + slot * N * P;
+  int rr = 0;
+  gemm<4, 4, false, false, kV>(rr, N, P, M, sm + L.Bt, N + kPad, sm + L.X, P + kPad,
+                               [&](int n, int pc, float v) { dH[n * P + pc] = v; });
+  gemm<4, 4, false, false, kV>(rr, N, P, M, sm + L.Ct, N + kPad, sm + L.dY, P + kPad,
+                               [&](int n, int pc, float v) { dG[n * P + pc] = v; });
+}
+
+// ------------------------------------------------------------------ chunk-level scans
+// One thread per (batch row, head, state pair kk, column p): rows 2 kk and 2 kk + 1 of the
+// state in column p.  blockIdx.y = 0: the folded entry states Hp(k), written over dH(k);
+// blockIdx.y = 1: the exit cotangents Gout(k), written over dG(k), and dh0.
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads) bwd_scan_kernel(const BwdParams p, long long total) {
+  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= total) return;
+  const int K = p.K, P = p.P, N = p.N, NP = N * P, nch = p.nch;
+  const int KP = K * P;
+  const int bh = static_cast<int>(idx / KP), rem = static_cast<int>(idx - static_cast<long long>(bh) * KP);
+  const int kk = rem / P, pc = rem - kk * P, n0 = 2 * kk;
+  const size_t base = static_cast<size_t>(bh) * nch * NP + static_cast<size_t>(n0) * P + pc;
+  const float* dec = p.wsDec + static_cast<size_t>(bh) * nch;
+  const float* sig = p.wsSig + static_cast<size_t>(bh) * nch * K + kk;
+  const float ph0 = p.phi0 ? wrap(p.phi0[static_cast<size_t>(bh) * K + kk]) : 0.f;
+  float s0, c0;
+  sincosf(ph0, &s0, &c0);
+  const size_t e0 = static_cast<size_t>(bh) * NP + static_cast<size_t>(n0) * P + pc;
+  if (blockIdx.y == 0) {
+    // Hp(0) in chunk 0's frame: R(-phi_0) h0 + q_0 prevB^T prevx (prevB is stored unrotated,
+    // which is its rotated value read in chunk 0's frame)
+    float a = 0.f, b = 0.f;
+    if (p.h0) {
+      a = p.h0[e0];
+      b = p.h0[e0 + P];
+    }
+    float H0 = c0 * a - s0 * b, H1 = s0 * a + c0 * b;
+    if (p.prevB0 && p.prevx0) {
+      const Tin* dtg = static_cast<const Tin*>(p.dt);
+      const Tin* lamg = static_cast<const Tin*>(p.lam);
+      const Tin* pB = static_cast<const Tin*>(p.prevB0);
+      const Tin* px = static_cast<const Tin*>(p.prevx0);
+      const size_t o = static_cast<size_t>(bh / p.H) * p.T * p.H + bh % p.H;
+      const float q0 = (1.f - to_f(lamg[o])) * to_f(dtg[o]);
+      float f0 = 0.f, f1 = 0.f;
+      for (int r = 0; r < p.R; ++r) {
+        const float xv = to_f(px[(static_cast<size_t>(bh) * p.R + r) * P + pc]);
+        f0 = fmaf(to_f(pB[(static_cast<size_t>(bh) * p.R + r) * N + n0]), xv, f0);
+        f1 = fmaf(to_f(pB[(static_cast<size_t>(bh) * p.R + r) * N + n0 + 1]), xv, f1);
+      }
+      H0 = fmaf(q0, f0, H0);
+      H1 = fmaf(q0, f1, H1);
+    }
+    float* hp = p.wsH + base;
+    float d0 = hp[0], d1 = hp[P];
+    for (int k = 0; k < nch; ++k) {
+      float n0v = 0.f, n1v = 0.f;
+      if (k + 1 < nch) {
+        n0v = hp[static_cast<size_t>(k + 1) * NP];
+        n1v = hp[static_cast<size_t>(k + 1) * NP + P];
+      }
+      hp[static_cast<size_t>(k) * NP] = H0;
+      hp[static_cast<size_t>(k) * NP + P] = H1;
+      if (k + 1 < nch) {
+        const float dk = dec[k];
+        float sn, cs;
+        sincosf(sig[static_cast<size_t>(k) * K], &sn, &cs);
+        const float X0 = fmaf(dk, H0, d0), X1 = fmaf(dk, H1, d1);
+        H0 = cs * X0 - sn * X1;
+        H1 = sn * X0 + cs * X1;
+      }
+      d0 = n0v;
+      d1 = n1v;
+    }
+  } else {
+    // the angle before the last chunk turns the exit cotangent into that chunk's frame
+    float ph = ph0;
+    for (int k = 0; k + 1 < nch; ++k) ph = wrap(ph + sig[static_cast<size_t>(k) * K]);
     float sn, cs;
     sincosf(ph, &sn, &cs);
-    for (int r = 0; r < R; ++r) {
-      float u = 0.f, v = 0.f;
-      if (p.prevB0) {
-        const Tin* q = static_cast<const Tin*>(p.prevB0) + (static_cast<size_t>(bh) * R + r) * N + 2 * k;
-        u = to_f(q[0]);
-        v = to_f(q[1]);
+    float a = 0.f, b = 0.f;
+    if (p.dhT) {
+      a = p.dhT[e0];
+      b = p.dhT[e0 + P];
+    }
+    float G0 = cs * a - sn * b, G1 = sn * a + cs * b;
+    float* gp = p.wsG + base;
+    float d0 = gp[static_cast<size_t>(nch - 1) * NP], d1 = gp[static_cast<size_t>(nch - 1) * NP + P];
+    for (int k = nch - 1; k >= 0; --k) {
+      float n0v = 0.f, n1v = 0.f;
+      if (k > 0) {
+        n0v = gp[static_cast<size_t>(k - 1) * NP];
+        n1v = gp[static_cast<size_t>(k - 1) * NP + P];
       }
-      s_pB[r * N + 2 * k] = cs * u + sn * v;
-      s_pB[r * N + 2 * k + 1] = -sn * u + cs * v;
+      gp[static_cast<size_t>(k) * NP] = G0;
+      gp[static_cast<size_t>(k) * NP + P] = G1;
+      const float dk = dec[k];
+      const float Y0 = fmaf(dk, G0, d0), Y1 = fmaf(dk, G1, d1);  // dHp(k), chunk k's frame
+      if (k > 0) {
+        sincosf(sig[static_cast<size_t>(k - 1) * K], &sn, &cs);
+        G0 = cs * Y0 + sn * Y1;
+        G1 = cs * Y1 - sn * Y0;
+      } else {
+        p.wsDH0[e0] = Y0;
+        p.wsDH0[e0 + P] = Y1;
+        if (p.dh0) {  // back to the absolute frame: R(phi_0)
+          p.dh0[e0] = c0 * Y0 + s0 * Y1;
+          p.dh0[e0 + P] = c0 * Y1 - s0 * Y0;
+        }
+      }
+      d0 = n0v;
+      d1 = n1v;
     }
-  }
-  for (int e = threadIdx.x; e < R * P; e += blockDim.x)
-    s_pX[e] = p.prevx0 ? to_f(static_cast<const Tin*>(p.prevx0)[static_cast<size_t>(bh) * R * P + e]) : 0.f;
-  __syncthreads();
-
-  // ---------------------------------------------------------------- forward over chunks
-  for (int k = 0; k < p.nch; ++k) {
-    const int t0 = k * c, nt = min(c, p.T - t0);
-    const size_t tok0 = seq0 + static_cast<size_t>(t0) * tok_stride;
-    for (int kk = threadIdx.x; kk < K; kk += blockDim.x)
-      p.wsPhi[(static_cast<size_t>(bh) * p.nch + k) * K + kk] = s_phi[kk];
-    chunk_coefs<Tin>(p, dtg, lamg, tok0, tok_stride, nt, A, s_dt, s_lam, s_ell, s_el, s_gam, s_q);
-    stage_theta<Tin>(thg, tok0, tok_stride, nt, c, K, s_th);
-    __syncthreads();
-    chunk_angles(nt, K, s_dt, s_th, s_phi, s_cs, s_sn);
-    __syncthreads();
-    load_rotated<Tin>(Bg, tok0, tok_stride, nt, R, N, K, M, s_cs, s_sn, sBC, ldN);
-    load_rows<Tin>(xg, tok0, tok_stride, nt, R, P, M, sXY, ldP);
-    // Hp = H + q_0 B~_prev^T X_prev, stored
-    const float q0 = s_q[0];
-    float* hp = p.wsH + (static_cast<size_t>(bh) * p.nch + k) * NP;
-    for (int e = threadIdx.x; e < NP; e += blockDim.x) {
-      const int n = e / P, pc = e - n * P;
-      float f = 0.f;
-      for (int r = 0; r < R; ++r) f = fmaf(s_pB[r * N + n], s_pX[r * P + pc], f);
-      const float v = fmaf(q0, f, sH[n * ldP + pc]);
-      sH[n * ldP + pc] = v;
-      hp[e] = v;
-    }
-    __syncthreads();
-    // the chunk's last token becomes the previous token of the next chunk (unscaled copy)
-    const int last = nt - 1;
-    for (int e = threadIdx.x; e < R * N; e += blockDim.x) s_pB[e] = sBC[(last * R + e / N) * ldN + e % N];
-    for (int e = threadIdx.x; e < R * P; e += blockDim.x) s_pX[e] = sXY[(last * R + e / P) * ldP + e % P];
-    // rows of B~ scaled by their token's Mh[last, token]
-    if (threadIdx.x < c) {
-      const int t = threadIdx.x;
-      s_rs[t] = t > last ? 0.f
-              : t == last ? s_gam[t]
-                          : expf(s_ell[last] - s_ell[t]) * (s_gam[t] + s_q[t + 1]);
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < M * N; e += blockDim.x) sBC[(e / N) * ldN + e % N] *= s_rs[(e / N) / R];
-    __syncthreads();
-    // H <- exp(l_last) Hp + sum_s Mh[last, s] B~_s^T X_s
-    const float e_last = s_el[last];
-    sgemm<4, 4>(N, P, M, sBC, 1, ldN, sXY, ldP, 1,
-                [&](int n, int pc, float v) { sH[n * ldP + pc] = fmaf(e_last, sH[n * ldP + pc], v); });
-    __syncthreads();
-  }
-
-  // ---------------------------------------------------------------- reverse over chunks
-  for (int e = threadIdx.x; e < NP; e += blockDim.x)
-    sH[(e / P) * ldP + e % P] = p.dhT ? p.dhT[static_cast<size_t>(bh) * NP + e] : 0.f;
-  __syncthreads();
-  for (int k = p.nch - 1; k >= 0; --k) {
-    const int t0 = k * c, nt = min(c, p.T - t0);
-    const size_t tok0 = seq0 + static_cast<size_t>(t0) * tok_stride;
-    for (int kk = threadIdx.x; kk < K; kk += blockDim.x)
-      s_phi[kk] = p.wsPhi[(static_cast<size_t>(bh) * p.nch + k) * K + kk];
-    chunk_coefs<Tin>(p, dtg, lamg, tok0, tok_stride, nt, A, s_dt, s_lam, s_ell, s_el, s_gam, s_q);
-    stage_theta<Tin>(thg, tok0, tok_stride, nt, c, K, s_th);
-    __syncthreads();
-    chunk_angles(nt, K, s_dt, s_th, s_phi, s_cs, s_sn);
-    __syncthreads();
-    load_rotated<Tin>(Cg, tok0, tok_stride, nt, R, N, K, M, s_cs, s_sn, sBC, ldN);
-    load_rows<Tdy>(dyg, tok0, tok_stride, nt, R, P, M, sXY, ldP);
-    float* go = p.wsG + (static_cast<size_t>(bh) * p.nch + k) * NP;
-    for (int e = threadIdx.x; e < NP; e += blockDim.x) go[e] = sH[(e / P) * ldP + e % P];
-    __syncthreads();
-    // rows of C~ scaled by exp(l) of their token
-    for (int e = threadIdx.x; e < M * N; e += blockDim.x) sBC[(e / N) * ldN + e % N] *= s_el[(e / N) / R];
-    __syncthreads();
-    // G <- exp(l_last) G + sum_i exp(l_i) C~_i^T dY_i
-    const float e_last = s_el[nt - 1];
-    sgemm<4, 4>(N, P, M, sBC, 1, ldN, sXY, ldP, 1,
-                [&](int n, int pc, float v) { sH[n * ldP + pc] = fmaf(e_last, sH[n * ldP + pc], v); });
-    __syncthreads();
-  }
-  for (int e = threadIdx.x; e < NP; e += blockDim.x) {
-    const float v = sH[(e / P) * ldP + e % P];
-    p.wsDH0[static_cast<size_t>(bh) * NP + e] = v;
-    if (p.dh0) p.dh0[static_cast<size_t>(bh) * NP + e] = v;
   }
 }
 
 // ------------------------------------------------------------------ per-chunk adjoint
-template <typename Tin, typename Tdy>
+template <typename Tin, typename Tdy, bool kV>
 __global__ void __launch_bounds__(kThreads) bwd_chunk_kernel(const BwdParams p) {
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   const int bh = blockIdx.x / p.nch, k = blockIdx.x % p.nch;
-  const int b = bh / p.H, head = bh % p.H;
+  const ChunkPos q = chunk_pos(p, bh, k);
   const int N = p.N, P = p.P, R = p.R, c = p.c, M = p.M, K = p.K, NP = N * P;
-  const ChunkSmem L = chunk_smem(N, P, R, c);
+  const int ldN = N + kPad, ldP = P + kPad, ldM = M + kPad, ldT = c + 1;
+  const ChunkSmem S = chunk_smem(N, P, R, c, sizeof(Tin), sizeof(Tdy));
+  const InSmem& L = S.in;
+  const size_t slot = static_cast<size_t>(bh) * p.nch + k;
+  const size_t tstride = p.H;
+  const float A = p.A[bh % p.H];
   float* sBt = sm + L.Bt;
   float* sCt = sm + L.Ct;
   float* sX = sm + L.X;
   float* sdY = sm + L.dY;
-  float* sHp = sm + L.Hp;
-  float* sdBt = sm + L.dBt;  // may share Hp's buffer: written only after Hp's last read
-  float* sGo = sm + L.Go;
-  float* sS = sm + L.S;
-  float* sdphi = sm + L.dphi;
-  float* sE = sm + L.E;
-  float* sW = sm + L.W;
-  float* sdCt = sm + L.dCt;
-  float* s_dM = sm + L.dM;
-  float* s_Mh = sm + L.Mh;
-  float* s_ex = sm + L.ex;
-  float* s_rowel = sm + L.rowel;
-  float* s_wx = sm + L.wx;
-  float* s_th = sm + L.th;
-  float* s_cs = sm + L.cs;
-  float* s_sn = sm + L.sn;
-  float* s_pB = sm + L.prevB;
-  float* s_pX = sm + L.prevX;
-  float* s_phi = sm + L.phi;
-  float* s_dt = sm + L.dt;
-  float* s_lam = sm + L.lam;
-  float* s_ell = sm + L.ell;
-  float* s_el = sm + L.el;
-  float* s_gam = sm + L.gam;
-  float* s_q = sm + L.q;
-  float* s_dexp = sm + L.dexp;
-  float* s_dgam = sm + L.dgam;
-  float* s_dq = sm + L.dq;
-  float* s_dell = sm + L.dell;
-  float* s_red = sm + L.red;
-  const int ldN = N + kPad, ldP = P + kPad, ldM = M + kPad, ldT = kMaxTok + 1;
-  const size_t tok_stride = p.H;
-  const int t0 = k * c, nt = min(c, p.T - t0), last = nt - 1;
-  const size_t seq0 = static_cast<size_t>(b) * p.T * p.H + head;
-  const size_t tok0 = seq0 + static_cast<size_t>(t0) * tok_stride;
-  const Tin* Bg = static_cast<const Tin*>(p.B);
-  const Tin* Cg = static_cast<const Tin*>(p.C);
-  const Tin* xg = static_cast<const Tin*>(p.x);
-  const Tin* dtg = static_cast<const Tin*>(p.dt);
-  const Tin* lamg = static_cast<const Tin*>(p.lam);
-  const Tin* thg = static_cast<const Tin*>(p.theta);
-  const Tdy* dyg = static_cast<const Tdy*>(p.dy);
-  const float A = p.A[head];
-  const bool has_next = k + 1 < p.nch;
+  float* sQ = sm + S.Q;
+  float* sXG = sm + S.XG;
+  float* sW = sm + S.W;
+  float* sHp = sm + S.Hp;
+  float* sGo = sm + S.Go;
+  float* sS = sm + S.S;
+  float* sE = sm + S.E;
+  float* sdphi = sm + S.dphi;
+  float* s_Mh = sm + S.Mh;
+  float* s_ex = sm + S.ex;
+  float* s_dM = sm + S.dM;
+  float* s_dexp = sm + S.dexp;
+  float* s_wdot = sm + S.wdot;
+  float* s_dell = sm + S.dell;
+  float* s_dgam = sm + S.dgam;
+  float* s_dq = sm + S.dq;
+  float* s_red = sm + S.red;
+  const float* s_dt = sm + L.dt;
+  const float* s_lam = sm + L.lam;
+  const float* s_ell = sm + L.ell;
+  const float* s_el = sm + L.el;
+  const float* s_gam = sm + L.gam;
+  const float* s_q = sm + L.q;
+  const float* s_wx = sm + L.wx;
+  const float* s_rowel = sm + L.rowel;
+  const float* s_cs = sm + L.cs;
+  const float* s_sn = sm + L.sn;
+  const float* hp = p.wsH + slot * NP;
+  const float* go = p.wsG + slot * NP;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
 
-  // ---------------------------------------------------------------- inputs of the chunk
-  const float* phib = p.wsPhi + (static_cast<size_t>(bh) * p.nch + k) * K;
-  for (int kk = threadIdx.x; kk < K; kk += blockDim.x) s_phi[kk] = phib[kk];
-  chunk_coefs<Tin>(p, dtg, lamg, tok0, tok_stride, nt, A, s_dt, s_lam, s_ell, s_el, s_gam, s_q);
-  if (threadIdx.x == 0) {  // q of the next chunk's first token (its fold weighs our last token)
-    const size_t tn = tok0 + static_cast<size_t>(nt) * tok_stride;
-    s_q[kMaxTok] = has_next ? (1.f - to_f(lamg[tn])) * to_f(dtg[tn]) : 0.f;
-  }
-  // the previous token (the previous chunk's last, or the entry state's), rotated by its angle
-  for (int kk = threadIdx.x; kk < K; kk += blockDim.x) {
-    float sn, cs;
-    sincosf(phib[kk], &sn, &cs);
-    for (int r = 0; r < R; ++r) {
-      float u = 0.f, v = 0.f;
-      if (k > 0) {
-        const Tin* q = Bg + ((tok0 - tok_stride) * R + r) * N + 2 * kk;
-        u = to_f(q[0]);
-        v = to_f(q[1]);
-      } else if (p.prevB0) {
-        const Tin* q = static_cast<const Tin*>(p.prevB0) + (static_cast<size_t>(bh) * R + r) * N + 2 * kk;
-        u = to_f(q[0]);
-        v = to_f(q[1]);
-      }
-      s_pB[r * N + 2 * kk] = cs * u + sn * v;
-      s_pB[r * N + 2 * kk + 1] = -sn * u + cs * v;
-    }
-  }
-  for (int e = threadIdx.x; e < R * P; e += blockDim.x) {
-    float v = 0.f;
-    if (k > 0) v = to_f(xg[(tok0 - tok_stride) * R * P + e]);
-    else if (p.prevx0) v = to_f(static_cast<const Tin*>(p.prevx0)[static_cast<size_t>(bh) * R * P + e]);
-    s_pX[e] = v;
-  }
-  stage_theta<Tin>(thg, tok0, tok_stride, nt, c, K, s_th);
-  __syncthreads();
-  chunk_angles(nt, K, s_dt, s_th, s_phi, s_cs, s_sn);
-  __syncthreads();
-  load_rotated<Tin>(Bg, tok0, tok_stride, nt, R, N, K, M, s_cs, s_sn, sBt, ldN);
-  load_rotated<Tin>(Cg, tok0, tok_stride, nt, R, N, K, M, s_cs, s_sn, sCt, ldN);
-  load_rows<Tin>(xg, tok0, tok_stride, nt, R, P, M, sX, ldP);
-  load_rows<Tdy>(dyg, tok0, tok_stride, nt, R, P, M, sdY, ldP);
-  const float* hp = p.wsH + (static_cast<size_t>(bh) * p.nch + k) * NP;
-  const float* go = p.wsG + (static_cast<size_t>(bh) * p.nch + k) * NP;
-  stage(NP, [&](int e) { return hp[e]; }, [&](int e, float v) { sHp[(e / P) * ldP + e % P] = v; });
-  stage(NP, [&](int e) { return go[e]; }, [&](int e, float v) { sGo[(e / P) * ldP + e % P] = v; });
-  __syncthreads();
+  // ---------------------------------------------------------------- inputs, Hp and Gout
+  load_chunk<Tin, Tdy, kV>(
+      p, q, A, L, sm, nullptr,
+      [&] {
+        if constexpr (kV) {
+          const int per = P / 4;
+          for (int e = threadIdx.x; e < N * per; e += blockDim.x) {
+            const int n = e / per, col = (e - n * per) * 4;
+            cp_async16(sHp + n * ldP + col, hp + n * P + col);
+            cp_async16(sGo + n * ldP + col, go + n * P + col);
+          }
+        } else {
+          for (int e = threadIdx.x; e < NP; e += blockDim.x) {
+            const int n = e / P, col = e - n * P;
+            sHp[n * ldP + col] = hp[e];
+            sGo[n * ldP + col] = go[e];
+          }
+        }
+      },
+      [&] { row_weights(q, c, R, L, sm); }, false, false);
 
-  // tables of the chunk: exp(l_i - l_s) and the mask Mh[i, s] per token pair; per row, exp(l)
-  // of its token and its weight on the exit-state terms, Mh[last, s] plus q of the next
-  // chunk's first token for the rows of the last token (their trapezoid term is folded into
-  // the next chunk)
-  const float q_next = s_q[kMaxTok];
+  // ---------------------------------------------------------------- products with the inputs
+  // tables per token pair: exp(l_i - l_s) and Mh[i, s]
   for (int e = threadIdx.x; e < c * c; e += blockDim.x) {
     const int ti = e / c, ts = e - ti * c;
     float ex = 0.f, m = 0.f;
-    if (ts <= ti && ti < nt) {
+    if (ts <= ti && ti < q.nt) {
       ex = expf(s_ell[ti] - s_ell[ts]);
       m = ts == ti ? s_gam[ti] : ex * (s_gam[ts] + s_q[ts + 1]);
     }
     s_ex[ti * ldT + ts] = ex;
     s_Mh[ti * ldT + ts] = m;
   }
-  __syncthreads();
-  for (int row = threadIdx.x; row < M; row += blockDim.x) {
-    const int t = row / R;
-    s_rowel[row] = s_el[t];
-    s_wx[row] = t < nt ? s_Mh[last * ldT + t] + (t == last && has_next ? q_next : 0.f) : 0.f;
+  {  // <Gout, Hp>, one partial per thread
+    float gh = 0.f;
+    for (int e = threadIdx.x; e < NP; e += blockDim.x) {
+      const int n = e / P, col = e - n * P;
+      gh = fmaf(sGo[n * ldP + col], sHp[n * ldP + col], gh);
+    }
+    s_red[threadIdx.x] = gh;
   }
+  int rr = 0;
+  // S = C~ B~^T, E = dY X^T, W = B~ Gout, Q = dY Hp^T, XG = X Gout^T
+  gemm<2, 4, true, true, kV>(rr, M, M, N, sCt, ldN, sBt, ldN,
+                             [&](int i, int s_, float v) { sS[i * ldM + s_] = v; });
+  gemm<2, 4, true, true, kV>(rr, M, M, P, sdY, ldP, sX, ldP,
+                             [&](int i, int s_, float v) { sE[i * ldM + s_] = v; });
+  gemm<4, 4, true, false, kV>(rr, M, P, N, sBt, ldN, sGo, ldP,
+                              [&](int s_, int pc, float v) { sW[s_ * ldP + pc] = v; });
+  gemm<4, 4, true, true, kV>(rr, M, N, P, sdY, ldP, sHp, ldP,
+                             [&](int i, int n, float v) { sQ[i * ldN + n] = v; });
+  gemm<4, 4, true, true, kV>(rr, M, N, P, sX, ldP, sGo, ldP,
+                             [&](int s_, int n, float v) { sXG[s_ * ldN + n] = v; });
+  __syncthreads();
 
-  // ---------------------------------------------------------------- S, E, W = B~ Gout
-  sgemm<2, 4>(M, M, N, sCt, ldN, 1, sBt, 1, ldN, [&](int i, int s_, float v) { sS[i * ldM + s_] = v; });
-  sgemm<2, 4>(M, M, P, sdY, ldP, 1, sX, 1, ldP, [&](int i, int s_, float v) { sE[i * ldM + s_] = v; });
-  sgemm<2, 4>(M, P, N, sBt, ldN, 1, sGo, ldP, 1, [&](int s_, int pc, float v) { sW[s_ * ldP + pc] = v; });
-  // <Gout, Hp>
-  float gh = 0.f;
-  for (int e = threadIdx.x; e < NP; e += blockDim.x) gh = fmaf(sGo[(e / P) * ldP + e % P], sHp[(e / P) * ldP + e % P], gh);
-  const float go_hp = block_sum(gh, s_red);  // (includes a barrier)
-
-  // ---------------------------------------------------------------- dMh per token pair
+  // ---------------------------------------------------------------- per token and token pair
+  // per token (a warp each): wdot_t = sum over its rows of <W, X> (= <Gout, B~_t^T X_t>),
+  // dexp_t = sum over its rows of <C~, Q> (+ <Gout, Hp> at the last token)
+  for (int t = warp; t < c; t += nw) {
+    float a = 0.f, b = 0.f;
+    if (t < q.nt) {
+      for (int e = lane; e < R * P; e += 32) {
+        const int row = t * R + e / P, col = e % P;
+        a = fmaf(sW[row * ldP + col], sX[row * ldP + col], a);
+      }
+      for (int e = lane; e < R * N; e += 32) {
+        const int row = t * R + e / N, col = e % N;
+        b = fmaf(sCt[row * ldN + col], sQ[row * ldN + col], b);
+      }
+      if (t == q.last)
+        for (int i = lane; i < static_cast<int>(blockDim.x); i += 32) b += s_red[i];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      a += __shfl_xor_sync(0xffffffffu, a, o);
+      b += __shfl_xor_sync(0xffffffffu, b, o);
+    }
+    if (lane == 0) {
+      s_wdot[t] = a;
+      s_dexp[t] = b;
+    }
+  }
+  // dMh per token pair (its R x R entries of S o E), then Mh o S and Mh o E in place
   for (int e = threadIdx.x; e < c * c; e += blockDim.x) {
     const int ti = e / c, ts = e - ti * c;
+    const float m = s_Mh[ti * ldT + ts];
     float v = 0.f;
-    if (ts <= ti && ti < nt) {
-      for (int r = 0; r < R; ++r)
-        for (int r2 = 0; r2 < R; ++r2) v = fmaf(sS[(ti * R + r) * ldM + ts * R + r2], sE[(ti * R + r) * ldM + ts * R + r2], v);
-      if (ti == last)  // the exit cotangent: <Gout, B~_s^T X_s>
-        for (int r2 = 0; r2 < R; ++r2)
-          for (int pc = 0; pc < P; ++pc) v = fmaf(sW[(ts * R + r2) * ldP + pc], sX[(ts * R + r2) * ldP + pc], v);
-    }
-    s_dM[ti * ldT + ts] = v;
+    for (int r = 0; r < R; ++r)
+      for (int r2 = 0; r2 < R; ++r2) {
+        const int o = (ti * R + r) * ldM + ts * R + r2;
+        const float sv = sS[o], ev = sE[o];
+        v = fmaf(sv, ev, v);
+        sS[o] = m * sv;
+        sE[o] = m * ev;
+      }
+    s_dM[ti * ldT + ts] = ts <= ti && ti < q.nt ? v : 0.f;
   }
   __syncthreads();
-  // Mh o S and Mh o E in place
-  for (int e = threadIdx.x; e < M * M; e += blockDim.x) {
-    const int i = e / M, s_ = e - i * M;
-    const float m = s_Mh[(i / R) * ldT + s_ / R];
-    sS[i * ldM + s_] *= m;
-    sE[i * ldM + s_] *= m;
-  }
-  // Q = dY Hp^T into dC~
-  sgemm<2, 4>(M, N, P, sdY, ldP, 1, sHp, 1, ldP, [&](int i, int n, float v) { sdCt[i * ldN + n] = v; });
-  __syncthreads();
-  // d exp(l_t) = sum over the token's rows of <C~_i, Q_i> (+ <Gout, Hp> at the last token)
-  for (int t = threadIdx.x; t < c; t += blockDim.x) {
-    float v = 0.f;
-    if (t < nt)
-      for (int r = 0; r < R; ++r)
-        for (int n = 0; n < N; ++n) v = fmaf(sCt[(t * R + r) * ldN + n], sdCt[(t * R + r) * ldN + n], v);
-    if (t == last) v += go_hp;
-    s_dexp[t] = v;
-  }
-  __syncthreads();  // Q read; Hp no longer read (dB~ may take its buffer)
-  // dC~ = D B~ + exp(l) Q
-  sgemm<2, 4>(M, N, M, sE, ldM, 1, sBt, ldN, 1,
-              [&](int i, int n, float v) { sdCt[i * ldN + n] = fmaf(s_rowel[i], sdCt[i * ldN + n], v); });
-  // dB~ = D^T C~ + wexit(s) X_s Gout^T  (the same thread owns an output in both products)
-  sgemm<2, 4>(M, N, M, sE, 1, ldM, sCt, ldN, 1, [&](int s_, int n, float v) { sdBt[s_ * ldN + n] = v; });
-  sgemm<2, 4>(M, N, P, sX, ldP, 1, sGo, 1, ldP,
-              [&](int s_, int n, float v) { sdBt[s_ * ldN + n] = fmaf(s_wx[s_], v, sdBt[s_ * ldN + n]); });
-  // dX = (Mh o S)^T dY + wexit(s) W_s  -> global
+
+  // ---------------------------------------------------------------- gradients of the rows
+  rr = 0;
+  // dC~ = (Mh o E) B~ + exp(l) Q, over Q
+  gemm<4, 4, true, false, kV>(rr, M, N, M, sE, ldM, sBt, ldN, [&](int i, int n, float v) {
+    sQ[i * ldN + n] = fmaf(s_rowel[i], sQ[i * ldN + n], v);
+  });
+  // dB~ = (Mh o E)^T C~ + wx X Gout^T, over XG
+  gemm<4, 4, false, false, kV>(rr, M, N, M, sE, ldM, sCt, ldN, [&](int s_, int n, float v) {
+    sXG[s_ * ldN + n] = fmaf(s_wx[s_], sXG[s_ * ldN + n], v);
+  });
+  // dX = (Mh o S)^T dY + wx W, to global
   float* dxg = p.dx;
-  sgemm<2, 4>(M, P, M, sS, 1, ldM, sdY, ldP, 1, [&](int s_, int pc, float v) {
+  gemm<4, 4, false, false, kV>(rr, M, P, M, sS, ldM, sdY, ldP, [&](int s_, int pc, float v) {
     const int ts = s_ / R;
-    if (ts < nt)
-      dxg[(tok0 + static_cast<size_t>(ts) * tok_stride) * R * P + (s_ - ts * R) * P + pc] =
+    if (ts < q.nt)
+      dxg[(q.tok0 + static_cast<size_t>(ts) * tstride) * R * P + static_cast<size_t>(s_ - ts * R) * P + pc] =
           fmaf(s_wx[s_], sW[s_ * ldP + pc], v);
   });
-  // the fold of this chunk's entry: dq_0 += <dHp(k), B~_prev^T X_prev>, dHp(k) = Gout(k - 1)
-  const float* dhp = k > 0 ? p.wsG + (static_cast<size_t>(bh) * p.nch + k - 1) * NP
-                           : p.wsDH0 + static_cast<size_t>(bh) * NP;
-  float fq = 0.f;
-  stage(NP, [&](int e) { return dhp[e]; }, [&](int e, float v) {
-    const int n = e / P, pc = e - n * P;
-    float f = 0.f;
-    for (int r = 0; r < R; ++r) f = fmaf(s_pB[r * N + n], s_pX[r * P + pc], f);
-    fq = fmaf(v, f, fq);
-  });
-  const float dq_fold = block_sum(fq, s_red);  // (includes a barrier)
-
-  // ---------------------------------------------------------------- mask and fold parameters
-  if (threadIdx.x < c) {
-    const int t = threadIdx.x;
+  // mask and fold parameters per token; the last row of dMh also carries the exit term
+  // <Gout, B~_s^T X_s> = wdot_s
+  for (int t = threadIdx.x; t < c; t += blockDim.x) {
     float dell = 0.f, dgam = 0.f, dq = 0.f;
-    if (t < nt) {
+    if (t < q.nt) {
+      auto dMf = [&](int ti, int ts) { return s_dM[ti * ldT + ts] + (ti == q.last ? s_wdot[ts] : 0.f); };
       dell = s_dexp[t] * s_el[t];
-      for (int ts = 0; ts < t; ++ts) dell = fmaf(s_dM[t * ldT + ts], s_Mh[t * ldT + ts], dell);  // row t
-      for (int ti = t + 1; ti < nt; ++ti) {  // column t: l_t, gamma_t, q_{t+1}
-        dell = fmaf(-s_dM[ti * ldT + t], s_Mh[ti * ldT + t], dell);
-        dgam = fmaf(s_dM[ti * ldT + t], s_ex[ti * ldT + t], dgam);
+      for (int ts = 0; ts < t; ++ts) dell = fmaf(dMf(t, ts), s_Mh[t * ldT + ts], dell);
+      for (int ti = t + 1; ti < q.nt; ++ti) {  // column t: l_t, gamma_t (through w_t)
+        const float d = dMf(ti, t);
+        dell = fmaf(-d, s_Mh[ti * ldT + t], dell);
+        dgam = fmaf(d, s_ex[ti * ldT + t], dgam);
       }
-      dgam += s_dM[t * ldT + t];
-      if (t == 0) {
-        dq = dq_fold;
-      } else {  // q_t weighs column t - 1
-        for (int ti = t; ti < nt; ++ti) dq = fmaf(s_dM[ti * ldT + t - 1], s_ex[ti * ldT + t - 1], dq);
-      }
+      dgam += dMf(t, t);
+      if (t > 0)  // q_t weighs column t - 1 (q_0's fold term is added later)
+        for (int ti = t; ti < q.nt; ++ti) dq = fmaf(dMf(ti, t - 1), s_ex[ti * ldT + t - 1], dq);
     }
     s_dell[t] = dell;
     s_dgam[t] = dgam;
@@ -691,107 +897,147 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_kernel(const BwdParams p) 
   }
   __syncthreads();
 
-  // ---------------------------------------------------------------- rotation adjoint, d phi
-  for (int e = threadIdx.x; e < c * K; e += blockDim.x) sdphi[e] = 0.f;
-  __syncthreads();
+  // ---------------------------------------------------------------- rotation adjoint
   float* dBg = p.dB;
   float* dCg = p.dC;
-  // one thread per (token, pair): its R rows in a fixed order
-  for (int e = threadIdx.x; e < nt * K; e += blockDim.x) {
+  for (int e = threadIdx.x; e < q.nt * K; e += blockDim.x) {  // one (token, pair), R rows in order
     const int t = e / K, kk = e - t * K;
     const float cs = s_cs[t * K + kk], sn = s_sn[t * K + kk];
     float dph = 0.f;
     for (int r = 0; r < R; ++r) {
       const int row = t * R + r;
-      const float db0 = sdBt[row * ldN + 2 * kk], db1 = sdBt[row * ldN + 2 * kk + 1];
-      const float dc0 = sdCt[row * ldN + 2 * kk], dc1 = sdCt[row * ldN + 2 * kk + 1];
+      const float db0 = sXG[row * ldN + 2 * kk], db1 = sXG[row * ldN + 2 * kk + 1];
+      const float dc0 = sQ[row * ldN + 2 * kk], dc1 = sQ[row * ldN + 2 * kk + 1];
       const float b0 = sBt[row * ldN + 2 * kk], b1 = sBt[row * ldN + 2 * kk + 1];
       const float c0 = sCt[row * ldN + 2 * kk], c1 = sCt[row * ldN + 2 * kk + 1];
-      const size_t o = ((tok0 + static_cast<size_t>(t) * tok_stride) * R + r) * N + 2 * kk;
-      dBg[o] = cs * db0 - sn * db1;
-      dBg[o + 1] = sn * db0 + cs * db1;
-      dCg[o] = cs * dc0 - sn * dc1;
-      dCg[o + 1] = sn * dc0 + cs * dc1;
+      const size_t o = ((q.tok0 + static_cast<size_t>(t) * tstride) * R + r) * N + 2 * kk;
+      *reinterpret_cast<float2*>(dBg + o) = make_float2(cs * db0 - sn * db1, sn * db0 + cs * db1);
+      *reinterpret_cast<float2*>(dCg + o) = make_float2(cs * dc0 - sn * dc1, sn * dc0 + cs * dc1);
       dph += db0 * b1 - db1 * b0 + dc0 * c1 - dc1 * c0;
     }
     sdphi[t * K + kk] = dph;
   }
+  if (threadIdx.x == 0 && q.has_next) p.wsDqf[slot + 1] = s_wdot[q.last];  // next chunk's fold
   __syncthreads();
-  // chunk-local suffix sums of d phi: d theta_t (this chunk's part) and their sum per pair
+  // chunk-local suffix sums of d phi: this chunk's part of d theta, and the chunk's total
+  const float* thraw = sm + L.th;
   for (int kk = threadIdx.x; kk < K; kk += blockDim.x) {
     float g = 0.f;
-    for (int t = nt - 1; t >= 0; --t) {
+    for (int t = q.nt - 1; t >= 0; --t) {
       g += sdphi[t * K + kk];
-      sdphi[t * K + kk] = g;
-      p.dtheta[(tok0 + static_cast<size_t>(t) * tok_stride) * K + kk] = s_dt[t] * g;
+      p.dtheta[(q.tok0 + static_cast<size_t>(t) * tstride) * K + kk] = s_dt[t] * g;
+      sdphi[t * K + kk] = g * theta_at<Tin, kV>(thraw, t * K + kk);  // theta . suffix, summed below
     }
-    p.wsSphi[(static_cast<size_t>(bh) * p.nch + k) * K + kk] = g;
+    p.wsSphi[slot * K + kk] = g;
   }
   __syncthreads();
-  // per token: d dt (this chunk's part of the angle term), d lambda; d(dt A) by a suffix sum
+  // per token: the angle term of d dt (a warp per token, pairs in a fixed order)
+  for (int t = warp; t < q.nt; t += nw) {
+    float v = 0.f;
+    for (int kk = lane; kk < K; kk += 32) v += sdphi[t * K + kk];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) s_dexp[t] = v;  // (dexp is no longer read)
+  }
+  __syncthreads();
   if (threadIdx.x < 32) {
     const int t = threadIdx.x;
     // d a_t = sum_{i >= t} d l_i (l_i = sum_{s <= i} a_s within the chunk)
-    float da = t < nt ? s_dell[t] : 0.f;
+    float da = t < q.nt ? s_dell[t] : 0.f;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const float v = __shfl_down_sync(0xffffffffu, da, o);
       if (t + o < 32) da += v;
     }
     float dadt = 0.f;
-    if (t < nt) {
-      float th = 0.f;
-      for (int kk = 0; kk < K; ++kk) th = fmaf(s_th[t * K + kk], sdphi[t * K + kk], th);
+    if (t < q.nt) {
       const float dt = s_dt[t], lam = s_lam[t];
-      const size_t o = tok0 + static_cast<size_t>(t) * tok_stride;
-      p.ddt[o] = th + da * A + lam * s_dgam[t] + (1.f - lam) * s_dq[t];
+      const size_t o = q.tok0 + static_cast<size_t>(t) * tstride;
+      p.ddt[o] = s_dexp[t] + da * A + lam * s_dgam[t] + (1.f - lam) * s_dq[t];
       p.dlam[o] = dt * (s_dgam[t] - s_dq[t]);
       dadt = da * dt;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) dadt += __shfl_xor_sync(0xffffffffu, dadt, o);
-    if (t == 0) p.wsDa[static_cast<size_t>(bh) * p.nch + k] = dadt;
+    if (t == 0) p.wsDa[slot] = dadt;
   }
 }
 
-// ------------------------------------------------------------------ angle carries, dA part
+// ------------------------------------------------------------------ carries across chunks
+// One CTA per (batch row, head): the d phi sums over chunks turned into sums over the chunks
+// after each one (in place), the (b, h) part of dA, and the fold gradient of the sequence's
+// first token, <dHp(0), prevB^T prevx> (chunk 0's frame, where prevB reads unrotated).
 template <typename Tin>
-__global__ void __launch_bounds__(kThreads) bwd_finalize_kernel(const BwdParams p) {
-  extern __shared__ float sm[];
-  const int bh = blockIdx.x, b = bh / p.H, head = bh % p.H;
-  const int K = p.K, c = p.c;
-  float* carry = sm;  // [K] sum of d phi over the chunks after the current one
-  const size_t tok_stride = p.H;
-  const size_t seq0 = static_cast<size_t>(b) * p.T * p.H + head;
-  const Tin* thg = static_cast<const Tin*>(p.theta);
-  const Tin* dtg = static_cast<const Tin*>(p.dt);
-  for (int kk = threadIdx.x; kk < K; kk += blockDim.x) carry[kk] = 0.f;
-  __syncthreads();
-  for (int k = p.nch - 1; k >= 0; --k) {
-    const int t0 = k * c, nt = min(c, p.T - t0);
-    const size_t tok0 = seq0 + static_cast<size_t>(t0) * tok_stride;
-    if (k + 1 < p.nch) {
-      for (int e = threadIdx.x; e < nt * K; e += blockDim.x) {
-        const int t = e / K, kk = e - t * K;
-        const size_t o = tok0 + static_cast<size_t>(t) * tok_stride;
-        p.dtheta[o * K + kk] = fmaf(to_f(dtg[o]), carry[kk], p.dtheta[o * K + kk]);
-      }
-      for (int t = threadIdx.x; t < nt; t += blockDim.x) {
-        const size_t o = tok0 + static_cast<size_t>(t) * tok_stride;
-        float v = 0.f;
-        for (int kk = 0; kk < K; ++kk) v = fmaf(to_f(thg[o * K + kk]), carry[kk], v);
-        p.ddt[o] += v;
-      }
+__global__ void __launch_bounds__(kThreads) bwd_carry_kernel(const BwdParams p) {
+  __shared__ float scratch[kThreads];
+  const int bh = blockIdx.x, K = p.K, nch = p.nch, N = p.N, P = p.P, R = p.R;
+  for (int kk = threadIdx.x; kk < K; kk += blockDim.x) {
+    float carry = 0.f;
+    for (int k = nch - 1; k >= 0; --k) {
+      float* s = p.wsSphi + (static_cast<size_t>(bh) * nch + k) * K + kk;
+      const float v = *s;
+      *s = carry;
+      carry += v;
     }
-    __syncthreads();
-    for (int kk = threadIdx.x; kk < K; kk += blockDim.x)
-      carry[kk] += p.wsSphi[(static_cast<size_t>(bh) * p.nch + k) * K + kk];
-    __syncthreads();
   }
   if (threadIdx.x == 0) {
     float s = 0.f;
-    for (int k = 0; k < p.nch; ++k) s += p.wsDa[static_cast<size_t>(bh) * p.nch + k];
+    for (int k = 0; k < nch; ++k) s += p.wsDa[static_cast<size_t>(bh) * nch + k];
     p.dApart[bh] = s;
+  }
+  float f = 0.f;
+  if (p.prevB0 && p.prevx0) {
+    const Tin* pB = static_cast<const Tin*>(p.prevB0) + static_cast<size_t>(bh) * R * N;
+    const Tin* px = static_cast<const Tin*>(p.prevx0) + static_cast<size_t>(bh) * R * P;
+    const float* g = p.wsDH0 + static_cast<size_t>(bh) * N * P;
+    for (int e = threadIdx.x; e < N * P; e += blockDim.x) {
+      const int n = e / P, pc = e - n * P;
+      float w = 0.f;
+      for (int r = 0; r < R; ++r) w = fmaf(to_f(pB[r * N + n]), to_f(px[r * P + pc]), w);
+      f = fmaf(g[e], w, f);
+    }
+  }
+  f = block_sum(f, scratch);
+  if (threadIdx.x == 0) p.wsDqf[static_cast<size_t>(bh) * nch] = f;
+}
+
+// One CTA per (batch row, head, chunk): d theta_t += dt_t carry, d dt_t += <theta_t, carry>
+// with carry the d phi of the chunks after this one; the chunk's first token takes its fold
+// gradient: d dt += (1 - lambda) dq, d lambda -= dt dq.
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads) bwd_apply_kernel(const BwdParams p) {
+  const int bh = blockIdx.x / p.nch, k = blockIdx.x % p.nch;
+  const ChunkPos q = chunk_pos(p, bh, k);
+  const int K = p.K;
+  const size_t slot = static_cast<size_t>(bh) * p.nch + k;
+  const Tin* dtg = static_cast<const Tin*>(p.dt);
+  const Tin* lamg = static_cast<const Tin*>(p.lam);
+  const Tin* thg = static_cast<const Tin*>(p.theta);
+  const float* carry = p.wsSphi + slot * K;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (q.has_next) {
+    for (int e = threadIdx.x; e < q.nt * K; e += blockDim.x) {
+      const int t = e / K, kk = e - t * K;
+      const size_t o = q.tok0 + static_cast<size_t>(t) * p.H;
+      p.dtheta[o * K + kk] = fmaf(to_f(dtg[o]), carry[kk], p.dtheta[o * K + kk]);
+    }
+  }
+  for (int t = warp; t < q.nt; t += nw) {
+    const size_t o = q.tok0 + static_cast<size_t>(t) * p.H;
+    float v = 0.f;
+    if (q.has_next)
+      for (int kk = lane; kk < K; kk += 32) v = fmaf(to_f(thg[o * K + kk]), carry[kk], v);
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+    if (lane == 0) {
+      float g = p.ddt[o] + v;
+      if (t == 0) {
+        const float dq = p.wsDqf[slot], dt = to_f(dtg[o]), lam = to_f(lamg[o]);
+        g = fmaf(1.f - lam, dq, g);
+        p.dlam[o] = fmaf(-dt, dq, p.dlam[o]);
+      }
+      p.ddt[o] = g;
+    }
   }
 }
 
@@ -811,18 +1057,44 @@ __global__ void copy_dh_kernel(const float* dhT, float* dh0, size_t n) {
     dh0[i] = dhT ? dhT[i] : 0.f;
 }
 
+int dtype_bytes(int dt) { return dt == M3_BF16 ? 2 : 4; }
+
 // Tokens per chunk: the largest of 32, 16, 8, 4, 2, 1 with at most 64 (token, rank) rows whose
-// per-chunk shared memory fits.
-constexpr size_t kSmemLimit = 200 * 1024;
+// shared memory fits one CTA of either per-chunk kernel.
+constexpr size_t kSmemLimit = 227 * 1024;
 int plan_c(const m3_dims& d) {
-  if (d.N * d.P > 8192) return 0;
+  if (d.N * d.P > 8192 || d.N % 2) return 0;
+  const int si = dtype_bytes(d.in_dtype), sy = dtype_bytes(d.out_dtype);
   for (int c = kMaxTok; c >= 1; c /= 2) {
     if (c * d.R > kMaxRows) continue;
-    if (static_cast<size_t>(chunk_smem(d.N, d.P, d.R, c).total) * 4 <= kSmemLimit &&
-        static_cast<size_t>(scan_smem(d.N, d.P, d.R, c).total) * 4 <= kSmemLimit)
+    if (static_cast<size_t>(chunk_smem(d.N, d.P, d.R, c, si, sy).total) * 4 <= kSmemLimit &&
+        static_cast<size_t>(local_smem(d.N, d.P, d.R, c, si, sy).total) * 4 <= kSmemLimit)
       return c;
   }
   return 0;
+}
+
+bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+template <typename Tin, typename Tdy, bool kV>
+cudaError_t launch_chunk_kernels(const BwdParams& p, size_t bhn, cudaStream_t s) {
+  const size_t sm1 = static_cast<size_t>(local_smem(p.N, p.P, p.R, p.c, sizeof(Tin), sizeof(Tdy)).total) * 4;
+  const size_t sm3 = static_cast<size_t>(chunk_smem(p.N, p.P, p.R, p.c, sizeof(Tin), sizeof(Tdy)).total) * 4;
+  auto k1 = bwd_local_kernel<Tin, Tdy, kV>;
+  auto k3 = bwd_chunk_kernel<Tin, Tdy, kV>;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)) != cudaSuccess)
+    return e;
+  const unsigned nblk = static_cast<unsigned>(bhn * p.nch);
+  k1<<<nblk, kThreads, sm1, s>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const long long total = static_cast<long long>(bhn) * p.K * p.P;
+  bwd_scan_kernel<Tin><<<dim3(static_cast<unsigned>((total + kThreads - 1) / kThreads), 2), kThreads, 0, s>>>(p, total);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  k3<<<nblk, kThreads, sm3, s>>>(p);
+  return cudaGetLastError();
 }
 
 template <typename Tin, typename Tdy>
@@ -859,12 +1131,14 @@ cudaError_t launch_bwd(const BackwardArgs& a, cudaStream_t s) {
   p.dlam = a.dlam;
   p.dtheta = a.dtheta;
   p.dh0 = a.dh0;
-  p.wsPhi = reinterpret_cast<float*>(a.ws + w.off_phi);
   p.wsH = reinterpret_cast<float*>(a.ws + w.off_h);
   p.wsG = reinterpret_cast<float*>(a.ws + w.off_g);
+  p.wsSig = reinterpret_cast<float*>(a.ws + w.off_sig);
+  p.wsDec = reinterpret_cast<float*>(a.ws + w.off_dec);
   p.wsDH0 = reinterpret_cast<float*>(a.ws + w.off_dh0);
   p.wsSphi = reinterpret_cast<float*>(a.ws + w.off_sphi);
   p.wsDa = reinterpret_cast<float*>(a.ws + w.off_da_chunk);
+  p.wsDqf = reinterpret_cast<float*>(a.ws + w.off_dqf);
   p.dApart = reinterpret_cast<float*>(a.ws + w.off_da);
   p.T = d.T;
   p.H = d.H;
@@ -875,19 +1149,14 @@ cudaError_t launch_bwd(const BackwardArgs& a, cudaStream_t s) {
   p.M = w.c * d.R;
   p.nch = w.nch;
   p.K = d.N / 2;
-  const size_t sm1 = static_cast<size_t>(scan_smem(d.N, d.P, d.R, w.c).total) * 4;
-  const size_t sm2 = static_cast<size_t>(chunk_smem(d.N, d.P, d.R, w.c).total) * 4;
-  auto k1 = bwd_scan_kernel<Tin, Tdy>;
-  auto k2 = bwd_chunk_kernel<Tin, Tdy>;
-  if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)) != cudaSuccess)
-    return e;
-  k1<<<static_cast<unsigned>(bhn), kThreads, sm1, s>>>(p);
+  // 16-byte copies and vector loads: row lengths of 16 bytes' multiples, aligned operands
+  const bool vec = d.N % 16 == 0 && d.P % 8 == 0 && p.M % 4 == 0 && aligned16(a.x) && aligned16(a.B) &&
+                   aligned16(a.C) && aligned16(a.theta) && aligned16(a.dy);
+  e = vec ? launch_chunk_kernels<Tin, Tdy, true>(p, bhn, s) : launch_chunk_kernels<Tin, Tdy, false>(p, bhn, s);
+  if (e != cudaSuccess) return e;
+  bwd_carry_kernel<Tin><<<static_cast<unsigned>(bhn), kThreads, 0, s>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  k2<<<static_cast<unsigned>(bhn * w.nch), kThreads, sm2, s>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bwd_finalize_kernel<Tin><<<static_cast<unsigned>(bhn), kThreads, sizeof(float) * p.K, s>>>(p);
+  bwd_apply_kernel<Tin><<<static_cast<unsigned>(bhn * w.nch), kThreads, 0, s>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   dA_reduce_kernel<<<(d.H + 127) / 128, 128, 0, s>>>(p.dApart, a.dA, d.B, d.H);
   return cudaGetLastError();
@@ -904,8 +1173,10 @@ BackwardWorkspace backward_workspace(const m3_dims& d) {
   auto up = [](size_t v) { return (v + 255) & ~size_t(255); };
   w.off_da = 256;
   w.off_da_chunk = w.off_da + up(bh * sizeof(float));
-  w.off_phi = w.off_da_chunk + up(bh * nch * sizeof(float));
-  w.off_sphi = w.off_phi + up(bh * nch * K * sizeof(float));
+  w.off_dec = w.off_da_chunk + up(bh * nch * sizeof(float));
+  w.off_dqf = w.off_dec + up(bh * nch * sizeof(float));
+  w.off_sig = w.off_dqf + up(bh * nch * sizeof(float));
+  w.off_sphi = w.off_sig + up(bh * nch * K * sizeof(float));
   w.off_dh0 = w.off_sphi + up(bh * nch * K * sizeof(float));
   w.off_h = w.off_dh0 + up(bh * np * sizeof(float));
   w.off_g = w.off_h + up(bh * nch * np * sizeof(float));

@@ -86,7 +86,7 @@ struct BackwardArgs {
 };
 struct BackwardWorkspace {
   int c, nch;  // tokens per chunk, chunks per sequence
-  size_t off_da, off_da_chunk, off_phi, off_sphi, off_dh0, off_h, off_g, bytes;
+  size_t off_da, off_da_chunk, off_dec, off_dqf, off_sig, off_sphi, off_dh0, off_h, off_g, bytes;
 };
 BackwardWorkspace backward_workspace(const m3_dims& d);
 bool backward_supported(const m3_dims& d);
