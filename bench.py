@@ -66,6 +66,28 @@ def prefill_bytes(w, out_bytes=4) -> int:
     return inp + out + state + w.H * 4
 
 
+B300_SMS = 148
+FP32_LANES_PER_SM = 128
+SM_MAX_MHZ = 2032
+BWD_CHUNK = 32  # tokens per chunk of the backward at (token, rank) rows <= 64
+
+
+def backward_fmas(w, c=BWD_CHUNK) -> int:
+    """fp32 multiply-adds of the chunked backward, dense M x M chunk products (M = c R rows):
+    per chunk 2 M N P (the chunk's own state terms) + 3 M N P (B~ Gout, dY Hp^T, X Gout^T)
+    + M^2 (3 N + 2 P) (C~ B~^T, dY X^T, dC~, dB~, dX)."""
+    while c * w.R > 64:
+        c //= 2
+    M = c * w.R
+    per_chunk = 5 * M * w.N * w.P + M * M * (3 * w.N + 2 * w.P)
+    return w.B * w.H * (w.T // c) * per_chunk
+
+
+def fp32_peak_tflops(mhz=SM_MAX_MHZ) -> float:
+    """CUDA-core fp32 peak: SMs x fp32 lanes x 2 flops per multiply-add x SM clock."""
+    return B300_SMS * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+
+
 def prefill_flops(w, rows=CHUNK_ROWS) -> int:
     """Flops of the chunked masked form at the kernel's chunk (full rows x rows score tiles)."""
     c_tok = rows // w.R
@@ -674,8 +696,8 @@ def main():
         del sx, ys, hs, ssteps, hsd
 
         # ---------------------------------------------------------- backward of the prefill
-        # Gradients of every input for the headline shape (fp32 CUDA-core adjoint recurrence
-        # with checkpoints); dy in fp32 like y.
+        # Gradients of every input for the headline shape (fp32 CUDA-core chunked adjoint: six
+        # launches); dy in fp32.
         dyb = torch.randn(w.B, w.T, w.H, w.R, w.P, dtype=torch.float32, device=dev)
         n_bws = m3.load().m3_ssm_prefill_backward_workspace(ctypes.byref(m3.M3Dims(
             w.B, w.T, w.H, w.P, w.N, w.R, 0, m3.M3_BF16, m3.M3_F32)))
@@ -691,12 +713,18 @@ def main():
         bb = tokh * (w.R * w.P * 2 + 2 * w.R * w.N * 2 + 2 * 2 + (w.N // 2) * 2   # inputs
                      + w.R * w.P * 4                                             # dy
                      + (w.R * w.P + 2 * w.R * w.N + 2 + w.N // 2) * 4) + w.H * 8 # gradients
+        fmab = backward_fmas(w)
         line["backward"] = {"workload": w.name, "ms": msb,
                             "tokens_per_s": D.aggregate_throughput(w.B * w.T, world, msb / 1e3),
+                            "bound": "alu",
+                            "fp32_fmas": fmab,
+                            "achieved_tflops": 2 * fmab / (msb / 1e3) / 1e12,
+                            "peak_tflops": fp32_peak_tflops(),
+                            "peak_source": "148 SMs x 128 fp32 lanes x 2 x 2032 MHz",
+                            "alu_frac": 2 * fmab / (msb / 1e3) / 1e12 / fp32_peak_tflops(),
                             "hbm_frac": bb / (msb / 1e3) / 1e9 / peaks["hbm_gbs"],
-                            "algorithmic_bytes": bb, "workspace_bytes": n_bws,
-                            "bound": "latency (one CTA per sequence, per-token barriers)"}
-        line["gpu_launches"] += 2 * 4
+                            "algorithmic_bytes": bb, "workspace_bytes": n_bws}
+        line["gpu_launches"] += 3 * 6  # three timed calls of six launches
         del dyb, wsb
 
         # ---------------------------------------------------------- 16384-token prefill + decode

@@ -272,13 +272,16 @@ m3_status m3_ssd_decode_step(const m3_dims* dims, float* h, const void* x_t, con
  *   dh0    float [B][H][N][P], gradient with respect to the entry state's h, or NULL.
  *          Gradients with respect to the entry state's angle and previous token are not
  *          produced.
- * All gradients are fp32 whatever the input dtype; the arithmetic is fp32 on CUDA cores
- * (one CTA per (batch row, head): a forward pass that stores the state every few tokens in
- * the workspace, then a reverse sweep that recomputes and walks back each stretch).
- * Supported when N * P <= 8192 (so that each thread holds at most 8 state rows of one
- * column); other shapes return M3_ERR_SHAPE.  Inputs, dtypes, alignment and stream
- * behaviour as m3_ssm_prefill; the workspace must hold m3_ssm_prefill_backward_workspace
- * bytes (its contents need no initialisation).  dims->chunk is ignored.
+ * All gradients are fp32 whatever the input dtype; the arithmetic is fp32 on CUDA cores in
+ * the chunked masked form, with chunks of up to 32 tokens (at most 64 (token, rank) rows):
+ * every chunk's own contributions to the states around it, in parallel over all chunks; a
+ * scan from chunk to chunk of the chunk-entry states and of the exit-state cotangents (fp32
+ * in the workspace, 2 N P floats per chunk); then every chunk's adjoint, in parallel.  Every
+ * reduction has a fixed order: results are bit-identical from run to run.  Supported when
+ * N * P <= 8192, N even and N <= 1024; other shapes return M3_ERR_SHAPE.  Inputs, dtypes,
+ * alignment and stream behaviour as m3_ssm_prefill; the workspace must hold
+ * m3_ssm_prefill_backward_workspace bytes (its contents need no initialisation).
+ * dims->chunk is ignored.
  */
 size_t m3_ssm_prefill_backward_workspace(const m3_dims* dims);
 

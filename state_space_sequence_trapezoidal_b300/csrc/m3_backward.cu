@@ -59,7 +59,8 @@ namespace {
 __device__ __forceinline__ float to_f(float v) { return v; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;       // threads of the local, carry and apply kernels
+constexpr int kThreadsChunk = 512;  // threads of the adjoint kernel
 constexpr int kPad = 4;        // floats of padding at the end of each shared-memory row
 constexpr int kMaxRows = 64;   // (token, rank) rows per chunk at most
 constexpr int kMaxTok = 32;    // tokens per chunk at most (one warp lane each)
@@ -99,6 +100,23 @@ struct BwdParams {
 
 __device__ __forceinline__ float wrap(float a) {
   return fmaf(-6.283185307179586f, rintf(a * 0.15915494309189535f), a);
+}
+
+// The chunk geometry.  Kernels specialised for a shape take compile-time values, which the
+// inlined helpers below fold into their index arithmetic; 0 means "from the parameters".
+struct Shape {
+  int N, P, R, c, K, M;
+};
+template <int SN, int SP, int SR, int SC>
+__device__ __forceinline__ Shape shape_of(const BwdParams& p) {
+  Shape s;
+  s.N = SN ? SN : p.N;
+  s.P = SP ? SP : p.P;
+  s.R = SR ? SR : p.R;
+  s.c = SC ? SC : p.c;
+  s.K = s.N / 2;
+  s.M = s.c * s.R;
+  return s;
 }
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
@@ -169,7 +187,7 @@ __device__ __forceinline__ void gemm(int& rr, int NI, int NJ, int NK, const floa
 #pragma unroll
       for (int v = 0; v < TJ; ++v) acc[u][v] = 0.f;
     if constexpr (kV) {
-#pragma unroll 2
+#pragma unroll 4
       for (int k0 = 0; k0 < NK; k0 += 4) {
         float av[4][TI], bv[4][TJ];
         if constexpr (kAK) {
@@ -264,6 +282,7 @@ struct InSmem {
   int th, cs, sn;                  // theta as loaded, cos / sin of psi [c][K]
   int dt, lam, ell, el, gam, q;    // per token (q: c + 1, the next chunk's first token last)
   int wx, rowel;                   // per row
+  int part;                        // scratch of the angle pass
 };
 __host__ __device__ inline void carve_inputs(Carve& cv, InSmem& s, int N, int P, int R, int c, int szIn,
                                              int szDy, int raw_at) {
@@ -283,6 +302,7 @@ __host__ __device__ inline void carve_inputs(Carve& cv, InSmem& s, int N, int P,
   s.q = cv.take(c + 1);
   s.wx = cv.take(M);
   s.rowel = cv.take(M);
+  s.part = cv.take(K > kThreadsChunk ? K : kThreadsChunk);
   // raw staging: at raw_at when given (an area free until the inputs are converted)
   Carve rc;
   rc.o = raw_at >= 0 ? raw_at : cv.o;
@@ -338,7 +358,7 @@ __host__ __device__ inline ChunkSmem chunk_smem(int N, int P, int R, int c, int 
   s.dell = cv.take(c);
   s.dgam = cv.take(c);
   s.dq = cv.take(c);
-  s.red = cv.take(kThreads);
+  s.red = cv.take(kThreadsChunk);
   s.total = cv.o;
   return s;
 }
@@ -349,12 +369,12 @@ struct ChunkPos {
   bool has_next;
   size_t tok0;  // index of (b, t0, h) in [B][T][H]
 };
-__device__ __forceinline__ ChunkPos chunk_pos(const BwdParams& p, int bh, int k) {
+__device__ __forceinline__ ChunkPos chunk_pos(const BwdParams& p, int bh, int k, int c) {
   ChunkPos q;
   const int b = bh / p.H, head = bh % p.H;
   q.k = k;
-  q.t0 = k * p.c;
-  q.nt = min(p.c, p.T - q.t0);
+  q.t0 = k * c;
+  q.nt = min(c, p.T - q.t0);
   q.last = q.nt - 1;
   q.has_next = k + 1 < p.nch;
   q.tok0 = (static_cast<size_t>(b) * p.T + q.t0) * p.H + head;
@@ -365,7 +385,7 @@ __device__ __forceinline__ ChunkPos chunk_pos(const BwdParams& p, int bh, int k)
 // rows of tokens >= nt zero.  kV: 16-byte asynchronous copies, straight into dst for fp32 or
 // into raw for 16-bit types (converted by finish_rows); else plain scalar loads.
 template <typename T, bool kV>
-__device__ void issue_rows(const T* src, const ChunkPos& q, size_t tok_stride, int c, int R, int len,
+__device__ __forceinline__ void issue_rows(const T* src, const ChunkPos& q, size_t tok_stride, int c, int R, int len,
                            float* dst, int ld, T* raw) {
   if constexpr (kV) {
     constexpr int vec = 16 / sizeof(T);
@@ -405,7 +425,7 @@ __device__ void issue_rows(const T* src, const ChunkPos& q, size_t tok_stride, i
 // After the copies have landed: each row's values (raw 16-bit staging, or dst in place),
 // rotated pairwise by the token's psi when rot, times rowscale[row] when given, into dst.
 template <typename T, bool kV>
-__device__ void finish_rows(const ChunkPos& q, int c, int R, int len, float* dst, int ld, const T* raw,
+__device__ __forceinline__ void finish_rows(const ChunkPos& q, int c, int R, int len, float* dst, int ld, const T* raw,
                             bool rot, const float* s_cs, const float* s_sn, int K, const float* rowscale) {
   constexpr bool kRaw = kV && sizeof(T) != 4;
   const int M = c * R;
@@ -446,7 +466,8 @@ __device__ void finish_rows(const ChunkPos& q, int c, int R, int len, float* dst
 // Per-token coefficients (warp 0, one lane per token, tokens >= nt zero): dt, lambda, the
 // chunk-local log-decay sums l, exp(l), gamma, q, and q of the next chunk's first token.
 template <typename Tin>
-__device__ void chunk_coefs(const BwdParams& p, const ChunkPos& q, float A, const InSmem& L, float* sm) {
+__device__ __forceinline__ void chunk_coefs(const BwdParams& p, const Shape& sh, const ChunkPos& q, float A,
+                                            const InSmem& L, float* sm) {
   if (threadIdx.x < 32) {
     const Tin* dtg = static_cast<const Tin*>(p.dt);
     const Tin* lamg = static_cast<const Tin*>(p.lam);
@@ -455,13 +476,19 @@ __device__ void chunk_coefs(const BwdParams& p, const ChunkPos& q, float A, cons
     const size_t o = q.tok0 + static_cast<size_t>(t) * p.H;
     const float dt = ok ? to_f(dtg[o]) : 0.f;
     const float lam = ok ? to_f(lamg[o]) : 0.f;
+    float dtn = 0.f, lamn = 0.f;  // the next chunk's first token, loaded with the others
+    if (t == 0 && q.has_next) {
+      const size_t tn = q.tok0 + static_cast<size_t>(q.nt) * p.H;
+      dtn = to_f(dtg[tn]);
+      lamn = to_f(lamg[tn]);
+    }
     float ell = dt * A;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
       const float v = __shfl_up_sync(0xffffffffu, ell, d);
       if (t >= d) ell += v;
     }
-    if (t < p.c) {
+    if (t < sh.c) {
       sm[L.dt + t] = dt;
       sm[L.lam + t] = lam;
       sm[L.ell + t] = ell;
@@ -469,18 +496,15 @@ __device__ void chunk_coefs(const BwdParams& p, const ChunkPos& q, float A, cons
       sm[L.gam + t] = lam * dt;
       sm[L.q + t] = (1.f - lam) * dt;
     }
-    if (t == 0) {
-      const size_t tn = q.tok0 + static_cast<size_t>(q.nt) * p.H;
-      sm[L.q + p.c] = q.has_next ? (1.f - to_f(lamg[tn])) * to_f(dtg[tn]) : 0.f;
-    }
+    if (t == 0) sm[L.q + sh.c] = (1.f - lamn) * dtn;
   }
 }
 
 // theta rows of the chunk into the th area (asynchronous copies when kV, else fp32 scalars).
 template <typename Tin, bool kV>
-__device__ void issue_theta(const BwdParams& p, const ChunkPos& q, float* s_th) {
+__device__ __forceinline__ void issue_theta(const BwdParams& p, const Shape& sh, const ChunkPos& q, float* s_th) {
   const Tin* thg = static_cast<const Tin*>(p.theta);
-  const int K = p.K;
+  const int K = sh.K;
   if constexpr (kV) {
     constexpr int vec = 16 / sizeof(Tin);
     const int per = K / vec, n = q.nt * per;
@@ -504,24 +528,42 @@ __device__ __forceinline__ float theta_at(const float* s_th, int e) {
     return s_th[e];
 }
 
-// psi_t = sum_{u <= t} dt_u theta_u from the chunk's start, reduced to [-pi, pi] at every
-// step, as cos / sin [c][K] (identity past nt); returns psi of the last token per pair.
+// psi_t = sum_{u <= t} dt_u theta_u from the chunk's start, reduced to [-pi, pi] after every
+// step, as cos / sin [c][K] (identity past nt); sig_out[kk] (when given) gets psi of the last
+// token.  The tokens are split into G segments with one thread per (pair, segment): the
+// reduced sum over each segment first, then every thread starts from the reduced sum of the
+// segments before its own and steps through its tokens.  Contains a barrier: every thread of
+// the CTA calls it.
 template <typename Tin, bool kV>
-__device__ void chunk_angles(const ChunkPos& q, int c, int K, const float* sm, const InSmem& L,
-                             float* s_cs, float* s_sn, float* sig_out) {
+__device__ __forceinline__ void chunk_angles(const ChunkPos& q, const Shape& sh, float* sm, const InSmem& L,
+                                             float* sig_out) {
+  const int K = sh.K, c = sh.c, nthr = blockDim.x;
   const float* s_th = sm + L.th;
-  for (int kk = threadIdx.x; kk < K; kk += blockDim.x) {
+  float* s_part = sm + L.part;
+  float* s_cs = sm + L.cs;
+  float* s_sn = sm + L.sn;
+  const int G = max(1, min(c, nthr / K)), per = (c + G - 1) / G;
+  for (int e = threadIdx.x; e < K * G; e += nthr) {
+    const int g = e / K, kk = e - g * K, t1 = min((g + 1) * per, q.nt);
     float ph = 0.f;
-    for (int t = 0; t < c; ++t) {
+    for (int t = g * per; t < t1; ++t) ph = wrap(fmaf(sm[L.dt + t], theta_at<Tin, kV>(s_th, t * K + kk), ph));
+    s_part[e] = ph;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < K * G; e += nthr) {
+    const int g = e / K, kk = e - g * K, t1 = min((g + 1) * per, c);
+    float ph = 0.f;
+    for (int h = 0; h < g; ++h) ph = wrap(ph + s_part[h * K + kk]);
+    for (int t = g * per; t < t1; ++t) {
       float sn = 0.f, cs = 1.f;
       if (t < q.nt) {
         ph = wrap(fmaf(sm[L.dt + t], theta_at<Tin, kV>(s_th, t * K + kk), ph));
         __sincosf(ph, &sn, &cs);
+        if (t == q.last && sig_out) sig_out[kk] = ph;
       }
       s_cs[t * K + kk] = cs;
       s_sn[t * K + kk] = sn;
     }
-    if (sig_out) sig_out[kk] = ph;
   }
 }
 
@@ -530,11 +572,12 @@ __device__ void chunk_angles(const ChunkPos& q, int c, int K, const float* sm, c
 // asynchronous copies with the inputs' (it runs after theta's copies are committed); the
 // function returns with every copy landed and a barrier passed.
 template <typename Tin, typename Tdy, bool kV, typename FX, typename FS>
-__device__ void load_chunk(const BwdParams& p, const ChunkPos& q, float A, const InSmem& L, float* sm,
-                           float* sig_out, FX extra, FS scales, bool scale_x, bool scale_y) {
-  const int N = p.N, P = p.P, R = p.R, c = p.c, K = p.K;
+__device__ __forceinline__ void load_chunk(const BwdParams& p, const Shape& sh, const ChunkPos& q, float A,
+                                           const InSmem& L, float* sm, float* sig_out, FX extra, FS scales,
+                                           bool scale_x, bool scale_y) {
+  const int N = sh.N, P = sh.P, R = sh.R, c = sh.c, K = sh.K;
   const size_t ts = p.H;
-  issue_theta<Tin, kV>(p, q, sm + L.th);
+  issue_theta<Tin, kV>(p, sh, q, sm + L.th);
   if constexpr (kV) cp_async_commit();
   issue_rows<Tin, kV>(static_cast<const Tin*>(p.B), q, ts, c, R, N, sm + L.Bt, N + kPad,
                       reinterpret_cast<Tin*>(sm + L.rB));
@@ -546,10 +589,10 @@ __device__ void load_chunk(const BwdParams& p, const ChunkPos& q, float A, const
                       reinterpret_cast<Tdy*>(sm + L.rY));
   extra();
   if constexpr (kV) cp_async_commit();
-  chunk_coefs<Tin>(p, q, A, L, sm);
+  chunk_coefs<Tin>(p, sh, q, A, L, sm);
   if constexpr (kV) asm volatile("cp.async.wait_group 1;" ::: "memory");
   __syncthreads();
-  chunk_angles<Tin, kV>(q, c, K, sm, L, sm + L.cs, sm + L.sn, sig_out);
+  chunk_angles<Tin, kV>(q, sh, sm, L, sig_out);
   scales();  // per-row weights from the coefficients
   if constexpr (kV) cp_async_wait_all();
   __syncthreads();
@@ -567,7 +610,7 @@ __device__ void load_chunk(const BwdParams& p, const ChunkPos& q, float A, const
 // Per row: wx, its weight on the exit-state terms (Mh[last, t], plus q of the next chunk's
 // first token for the last token, whose trapezoid term that chunk folds in), and exp(l) of
 // its token.  Needs the coefficients (a barrier after chunk_coefs).
-__device__ void row_weights(const ChunkPos& q, int c, int R, const InSmem& L, float* sm) {
+__device__ __forceinline__ void row_weights(const ChunkPos& q, int c, int R, const InSmem& L, float* sm) {
   for (int row = threadIdx.x; row < c * R; row += blockDim.x) {
     const int t = row / R;
     float wx = 0.f;
@@ -580,16 +623,17 @@ __device__ void row_weights(const ChunkPos& q, int c, int R, const InSmem& L, fl
 }
 
 // ------------------------------------------------------------------ chunk-local state terms
-template <typename Tin, typename Tdy, bool kV>
-__global__ void __launch_bounds__(kThreads) bwd_local_kernel(const BwdParams p) {
+template <typename Tin, typename Tdy, bool kV, int SN, int SP, int SR, int SC>
+__global__ void __launch_bounds__(kThreads, 2) bwd_local_kernel(const BwdParams p) {
   extern __shared__ __align__(16) float sm[];
+  const Shape sh = shape_of<SN, SP, SR, SC>(p);
+  const int N = sh.N, P = sh.P, R = sh.R, c = sh.c, M = sh.M, K = sh.K;
   const int bh = blockIdx.x / p.nch, k = blockIdx.x % p.nch;
-  const ChunkPos q = chunk_pos(p, bh, k);
-  const int N = p.N, P = p.P, R = p.R, c = p.c, M = p.M, K = p.K;
+  const ChunkPos q = chunk_pos(p, bh, k, c);
   const LocalSmem S = local_smem(N, P, R, c, sizeof(Tin), sizeof(Tdy));
   const InSmem& L = S.in;
   const size_t slot = static_cast<size_t>(bh) * p.nch + k;
-  load_chunk<Tin, Tdy, kV>(p, q, p.A[bh % p.H], L, sm, p.wsSig + slot * K, [] {},
+  load_chunk<Tin, Tdy, kV>(p, sh, q, p.A[bh % p.H], L, sm, p.wsSig + slot * K, [] {},
                            [&] { row_weights(q, c, R, L, sm); }, true, true);
   if (threadIdx.x == 0) p.wsDec[slot] = sm[L.el + q.last];
   // dH[n][p] = sum_s B~[s][n] (wx_s X[s][p]),  dG[n][p] = sum_i C~[i][n] (exp(l_i) dY[i][p])
@@ -710,12 +754,13 @@ __global__ void __launch_bounds__(kThreads) bwd_scan_kernel(const BwdParams p, l
 }
 
 // ------------------------------------------------------------------ per-chunk adjoint
-template <typename Tin, typename Tdy, bool kV>
-__global__ void __launch_bounds__(kThreads) bwd_chunk_kernel(const BwdParams p) {
+template <typename Tin, typename Tdy, bool kV, int SN, int SP, int SR, int SC>
+__global__ void __launch_bounds__(kThreadsChunk, 1) bwd_chunk_kernel(const BwdParams p) {
   extern __shared__ __align__(16) float sm[];
+  const Shape sh = shape_of<SN, SP, SR, SC>(p);
+  const int N = sh.N, P = sh.P, R = sh.R, c = sh.c, M = sh.M, K = sh.K, NP = N * P;
   const int bh = blockIdx.x / p.nch, k = blockIdx.x % p.nch;
-  const ChunkPos q = chunk_pos(p, bh, k);
-  const int N = p.N, P = p.P, R = p.R, c = p.c, M = p.M, K = p.K, NP = N * P;
+  const ChunkPos q = chunk_pos(p, bh, k, c);
   const int ldN = N + kPad, ldP = P + kPad, ldM = M + kPad, ldT = c + 1;
   const ChunkSmem S = chunk_smem(N, P, R, c, sizeof(Tin), sizeof(Tdy));
   const InSmem& L = S.in;
@@ -759,7 +804,7 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_kernel(const BwdParams p) 
 
   // ---------------------------------------------------------------- inputs, Hp and Gout
   load_chunk<Tin, Tdy, kV>(
-      p, q, A, L, sm, nullptr,
+      p, sh, q, A, L, sm, nullptr,
       [&] {
         if constexpr (kV) {
           const int per = P / 4;
@@ -799,17 +844,18 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_kernel(const BwdParams p) 
     s_red[threadIdx.x] = gh;
   }
   int rr = 0;
-  // S = C~ B~^T, E = dY X^T, W = B~ Gout, Q = dY Hp^T, XG = X Gout^T
+  // W = B~ Gout, S = C~ B~^T, Q = dY Hp^T, XG = X Gout^T, E = dY X^T (tiles of about equal
+  // work, the largest products first)
+  gemm<2, 4, true, false, kV>(rr, M, P, N, sBt, ldN, sGo, ldP,
+                              [&](int s_, int pc, float v) { sW[s_ * ldP + pc] = v; });
   gemm<2, 4, true, true, kV>(rr, M, M, N, sCt, ldN, sBt, ldN,
                              [&](int i, int s_, float v) { sS[i * ldM + s_] = v; });
-  gemm<2, 4, true, true, kV>(rr, M, M, P, sdY, ldP, sX, ldP,
-                             [&](int i, int s_, float v) { sE[i * ldM + s_] = v; });
-  gemm<4, 4, true, false, kV>(rr, M, P, N, sBt, ldN, sGo, ldP,
-                              [&](int s_, int pc, float v) { sW[s_ * ldP + pc] = v; });
   gemm<4, 4, true, true, kV>(rr, M, N, P, sdY, ldP, sHp, ldP,
                              [&](int i, int n, float v) { sQ[i * ldN + n] = v; });
   gemm<4, 4, true, true, kV>(rr, M, N, P, sX, ldP, sGo, ldP,
                              [&](int s_, int n, float v) { sXG[s_ * ldN + n] = v; });
+  gemm<2, 4, true, true, kV>(rr, M, M, P, sdY, ldP, sX, ldP,
+                             [&](int i, int s_, float v) { sE[i * ldM + s_] = v; });
   __syncthreads();
 
   // ---------------------------------------------------------------- per token and token pair
@@ -859,48 +905,57 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_kernel(const BwdParams p) 
   // ---------------------------------------------------------------- gradients of the rows
   rr = 0;
   // dC~ = (Mh o E) B~ + exp(l) Q, over Q
-  gemm<4, 4, true, false, kV>(rr, M, N, M, sE, ldM, sBt, ldN, [&](int i, int n, float v) {
+  gemm<2, 4, true, false, kV>(rr, M, N, M, sE, ldM, sBt, ldN, [&](int i, int n, float v) {
     sQ[i * ldN + n] = fmaf(s_rowel[i], sQ[i * ldN + n], v);
   });
   // dB~ = (Mh o E)^T C~ + wx X Gout^T, over XG
-  gemm<4, 4, false, false, kV>(rr, M, N, M, sE, ldM, sCt, ldN, [&](int s_, int n, float v) {
+  gemm<2, 4, false, false, kV>(rr, M, N, M, sE, ldM, sCt, ldN, [&](int s_, int n, float v) {
     sXG[s_ * ldN + n] = fmaf(s_wx[s_], sXG[s_ * ldN + n], v);
   });
   // dX = (Mh o S)^T dY + wx W, to global
   float* dxg = p.dx;
-  gemm<4, 4, false, false, kV>(rr, M, P, M, sS, ldM, sdY, ldP, [&](int s_, int pc, float v) {
+  gemm<2, 4, false, false, kV>(rr, M, P, M, sS, ldM, sdY, ldP, [&](int s_, int pc, float v) {
     const int ts = s_ / R;
     if (ts < q.nt)
       dxg[(q.tok0 + static_cast<size_t>(ts) * tstride) * R * P + static_cast<size_t>(s_ - ts * R) * P + pc] =
           fmaf(s_wx[s_], sW[s_ * ldP + pc], v);
   });
-  // mask and fold parameters per token; the last row of dMh also carries the exit term
-  // <Gout, B~_s^T X_s> = wdot_s
-  for (int t = threadIdx.x; t < c; t += blockDim.x) {
-    float dell = 0.f, dgam = 0.f, dq = 0.f;
-    if (t < q.nt) {
-      auto dMf = [&](int ti, int ts) { return s_dM[ti * ldT + ts] + (ti == q.last ? s_wdot[ts] : 0.f); };
-      dell = s_dexp[t] * s_el[t];
-      for (int ts = 0; ts < t; ++ts) dell = fmaf(dMf(t, ts), s_Mh[t * ldT + ts], dell);
-      for (int ti = t + 1; ti < q.nt; ++ti) {  // column t: l_t, gamma_t (through w_t)
-        const float d = dMf(ti, t);
-        dell = fmaf(-d, s_Mh[ti * ldT + t], dell);
-        dgam = fmaf(d, s_ex[ti * ldT + t], dgam);
-      }
-      dgam += dMf(t, t);
-      if (t > 0)  // q_t weighs column t - 1 (q_0's fold term is added later)
-        for (int ti = t; ti < q.nt; ++ti) dq = fmaf(dMf(ti, t - 1), s_ex[ti * ldT + t - 1], dq);
-    }
-    s_dell[t] = dell;
-    s_dgam[t] = dgam;
-    s_dq[t] = dq;
-  }
   __syncthreads();
 
   // ---------------------------------------------------------------- rotation adjoint
+  // the mask and fold parameters per token, a warp each, lanes over the other token (the last
+  // row of dMh also carries the exit term <Gout, B~_s^T X_s> = wdot_s)
+  for (int t = warp; t < c; t += nw) {
+    auto dMf = [&](int ti, int ts) { return s_dM[ti * ldT + ts] + (ti == q.last ? s_wdot[ts] : 0.f); };
+    const int j = lane;
+    float rw = 0.f, cl = 0.f, cg = 0.f, cq = 0.f;
+    if (t < q.nt && j < q.nt) {
+      if (j < t) rw = dMf(t, j) * s_Mh[t * ldT + j];  // row t: l_t
+      if (j > t) {                                    // column t: l_t, gamma_t (through w_t)
+        const float d = dMf(j, t);
+        cl = d * s_Mh[j * ldT + t];
+        cg = d * s_ex[j * ldT + t];
+      }
+      if (t > 0 && j >= t) cq = dMf(j, t - 1) * s_ex[j * ldT + t - 1];  // q_t weighs column t - 1
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      rw += __shfl_xor_sync(0xffffffffu, rw, o);
+      cl += __shfl_xor_sync(0xffffffffu, cl, o);
+      cg += __shfl_xor_sync(0xffffffffu, cg, o);
+      cq += __shfl_xor_sync(0xffffffffu, cq, o);
+    }
+    if (lane == 0) {
+      const bool ok = t < q.nt;
+      s_dell[t] = ok ? fmaf(s_dexp[t], s_el[t], rw - cl) : 0.f;
+      s_dgam[t] = ok ? cg + dMf(t, t) : 0.f;
+      s_dq[t] = ok ? cq : 0.f;  // q_0's fold term is added later
+    }
+  }
+  // the rotation adjoint
   float* dBg = p.dB;
   float* dCg = p.dC;
-  for (int e = threadIdx.x; e < q.nt * K; e += blockDim.x) {  // one (token, pair), R rows in order
+  for (int e = threadIdx.x; e < q.nt * K; e += blockDim.x) {  // a (token, pair), its R rows in order
     const int t = e / K, kk = e - t * K;
     const float cs = s_cs[t * K + kk], sn = s_sn[t * K + kk];
     float dph = 0.f;
@@ -919,16 +974,30 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_kernel(const BwdParams p) 
   }
   if (threadIdx.x == 0 && q.has_next) p.wsDqf[slot + 1] = s_wdot[q.last];  // next chunk's fold
   __syncthreads();
-  // chunk-local suffix sums of d phi: this chunk's part of d theta, and the chunk's total
+  // chunk-local suffix sums of d phi: this chunk's part of d theta, and the chunk's total.  The
+  // tokens are split into G segments, one thread per (pair, segment): each segment's sum, then
+  // every thread starts from the sum of the later segments and walks its tokens backwards.
   const float* thraw = sm + L.th;
-  for (int kk = threadIdx.x; kk < K; kk += blockDim.x) {
-    float g = 0.f;
-    for (int t = q.nt - 1; t >= 0; --t) {
-      g += sdphi[t * K + kk];
-      p.dtheta[(q.tok0 + static_cast<size_t>(t) * tstride) * K + kk] = s_dt[t] * g;
-      sdphi[t * K + kk] = g * theta_at<Tin, kV>(thraw, t * K + kk);  // theta . suffix, summed below
+  {
+    const int G = max(1, min(c, static_cast<int>(blockDim.x) / K)), per = (c + G - 1) / G;
+    for (int e = threadIdx.x; e < K * G; e += blockDim.x) {
+      const int g = e / K, kk = e - g * K, t1 = min((g + 1) * per, q.nt);
+      float v = 0.f;
+      for (int t = g * per; t < t1; ++t) v += sdphi[t * K + kk];
+      s_red[e] = v;
     }
-    p.wsSphi[slot * K + kk] = g;
+    __syncthreads();
+    for (int e = threadIdx.x; e < K * G; e += blockDim.x) {
+      const int g = e / K, kk = e - g * K, t1 = min((g + 1) * per, q.nt);
+      float v = 0.f;
+      for (int h = G - 1; h > g; --h) v += s_red[h * K + kk];
+      for (int t = t1 - 1; t >= g * per; --t) {
+        v += sdphi[t * K + kk];
+        p.dtheta[(q.tok0 + static_cast<size_t>(t) * tstride) * K + kk] = s_dt[t] * v;
+        sdphi[t * K + kk] = v * theta_at<Tin, kV>(thraw, t * K + kk);  // theta . suffix, summed below
+      }
+      if (g == 0) p.wsSphi[slot * K + kk] = v;
+    }
   }
   __syncthreads();
   // per token: the angle term of d dt (a warp per token, pairs in a fixed order)
@@ -1003,11 +1072,12 @@ __global__ void __launch_bounds__(kThreads) bwd_carry_kernel(const BwdParams p) 
 
 // One CTA per (batch row, head, chunk): d theta_t += dt_t carry, d dt_t += <theta_t, carry>
 // with carry the d phi of the chunks after this one; the chunk's first token takes its fold
-// gradient: d dt += (1 - lambda) dq, d lambda -= dt dq.
-template <typename Tin>
+// gradient: d dt += (1 - lambda) dq, d lambda -= dt dq.  kQ: K / 4 divides 32 and the pairs are
+// taken four at a time (16-byte loads and stores), the K / 4 lanes of a token in one warp.
+template <typename Tin, bool kQ>
 __global__ void __launch_bounds__(kThreads) bwd_apply_kernel(const BwdParams p) {
   const int bh = blockIdx.x / p.nch, k = blockIdx.x % p.nch;
-  const ChunkPos q = chunk_pos(p, bh, k);
+  const ChunkPos q = chunk_pos(p, bh, k, p.c);
   const int K = p.K;
   const size_t slot = static_cast<size_t>(bh) * p.nch + k;
   const Tin* dtg = static_cast<const Tin*>(p.dt);
@@ -1015,28 +1085,64 @@ __global__ void __launch_bounds__(kThreads) bwd_apply_kernel(const BwdParams p) 
   const Tin* thg = static_cast<const Tin*>(p.theta);
   const float* carry = p.wsSphi + slot * K;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  if (q.has_next) {
-    for (int e = threadIdx.x; e < q.nt * K; e += blockDim.x) {
-      const int t = e / K, kk = e - t * K;
-      const size_t o = q.tok0 + static_cast<size_t>(t) * p.H;
-      p.dtheta[o * K + kk] = fmaf(to_f(dtg[o]), carry[kk], p.dtheta[o * K + kk]);
-    }
-  }
-  for (int t = warp; t < q.nt; t += nw) {
+  // the token's fold gradient and angle term, added by the lane that owns its first pairs
+  auto finish = [&](int t, float v) {
     const size_t o = q.tok0 + static_cast<size_t>(t) * p.H;
-    float v = 0.f;
-    if (q.has_next)
-      for (int kk = lane; kk < K; kk += 32) v = fmaf(to_f(thg[o * K + kk]), carry[kk], v);
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
-    if (lane == 0) {
-      float g = p.ddt[o] + v;
-      if (t == 0) {
-        const float dq = p.wsDqf[slot], dt = to_f(dtg[o]), lam = to_f(lamg[o]);
-        g = fmaf(1.f - lam, dq, g);
-        p.dlam[o] = fmaf(-dt, dq, p.dlam[o]);
+    float g = p.ddt[o] + v;
+    if (t == 0) {
+      const float dq = p.wsDqf[slot], dt = to_f(dtg[o]), lam = to_f(lamg[o]);
+      g = fmaf(1.f - lam, dq, g);
+      p.dlam[o] = fmaf(-dt, dq, p.dlam[o]);
+    }
+    p.ddt[o] = g;
+  };
+  if constexpr (kQ) {
+    const int KQ = K / 4, n = q.nt * KQ;
+    for (int e0 = 0; e0 < n; e0 += blockDim.x) {
+      const int e = e0 + threadIdx.x, t = e / KQ, j = e - t * KQ;
+      float v = 0.f;
+      if (e < n && q.has_next) {
+        const size_t o = q.tok0 + static_cast<size_t>(t) * p.H;
+        const float4 cr = *reinterpret_cast<const float4*>(carry + 4 * j);
+        float th[4];
+        if constexpr (sizeof(Tin) == 4) {
+          const float4 tv = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(thg) + o * K + 4 * j);
+          th[0] = tv.x, th[1] = tv.y, th[2] = tv.z, th[3] = tv.w;
+        } else {
+          const uint2 tv = *reinterpret_cast<const uint2*>(thg + o * K + 4 * j);
+          const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&tv.x));
+          const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&tv.y));
+          th[0] = lo.x, th[1] = lo.y, th[2] = hi.x, th[3] = hi.y;
+        }
+        const float dt = to_f(dtg[o]);
+        float4* dth = reinterpret_cast<float4*>(p.dtheta + o * K + 4 * j);
+        float4 d = *dth;
+        d.x = fmaf(dt, cr.x, d.x);
+        d.y = fmaf(dt, cr.y, d.y);
+        d.z = fmaf(dt, cr.z, d.z);
+        d.w = fmaf(dt, cr.w, d.w);
+        *dth = d;
+        v = fmaf(th[0], cr.x, fmaf(th[1], cr.y, fmaf(th[2], cr.z, th[3] * cr.w)));
       }
-      p.ddt[o] = g;
+      for (int o = KQ / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (e < n && j == 0) finish(t, v);
+    }
+  } else {
+    if (q.has_next) {
+      for (int e = threadIdx.x; e < q.nt * K; e += blockDim.x) {
+        const int t = e / K, kk = e - t * K;
+        const size_t o = q.tok0 + static_cast<size_t>(t) * p.H;
+        p.dtheta[o * K + kk] = fmaf(to_f(dtg[o]), carry[kk], p.dtheta[o * K + kk]);
+      }
+    }
+    for (int t = warp; t < q.nt; t += nw) {
+      const size_t o = q.tok0 + static_cast<size_t>(t) * p.H;
+      float v = 0.f;
+      if (q.has_next)
+        for (int kk = lane; kk < K; kk += 32) v = fmaf(to_f(thg[o * K + kk]), carry[kk], v);
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+      if (lane == 0) finish(t, v);
     }
   }
 }
@@ -1063,7 +1169,7 @@ int dtype_bytes(int dt) { return dt == M3_BF16 ? 2 : 4; }
 // shared memory fits one CTA of either per-chunk kernel.
 constexpr size_t kSmemLimit = 227 * 1024;
 int plan_c(const m3_dims& d) {
-  if (d.N * d.P > 8192 || d.N % 2) return 0;
+  if (d.N * d.P > 8192 || d.N % 2 || d.N > 2 * kThreadsChunk) return 0;
   const int si = dtype_bytes(d.in_dtype), sy = dtype_bytes(d.out_dtype);
   for (int c = kMaxTok; c >= 1; c /= 2) {
     if (c * d.R > kMaxRows) continue;
@@ -1076,12 +1182,12 @@ int plan_c(const m3_dims& d) {
 
 bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-template <typename Tin, typename Tdy, bool kV>
+template <typename Tin, typename Tdy, bool kV, int SN, int SP, int SR, int SC>
 cudaError_t launch_chunk_kernels(const BwdParams& p, size_t bhn, cudaStream_t s) {
   const size_t sm1 = static_cast<size_t>(local_smem(p.N, p.P, p.R, p.c, sizeof(Tin), sizeof(Tdy)).total) * 4;
   const size_t sm3 = static_cast<size_t>(chunk_smem(p.N, p.P, p.R, p.c, sizeof(Tin), sizeof(Tdy)).total) * 4;
-  auto k1 = bwd_local_kernel<Tin, Tdy, kV>;
-  auto k3 = bwd_chunk_kernel<Tin, Tdy, kV>;
+  auto k1 = bwd_local_kernel<Tin, Tdy, kV, SN, SP, SR, SC>;
+  auto k3 = bwd_chunk_kernel<Tin, Tdy, kV, SN, SP, SR, SC>;
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) != cudaSuccess)
     return e;
@@ -1093,7 +1199,7 @@ cudaError_t launch_chunk_kernels(const BwdParams& p, size_t bhn, cudaStream_t s)
   const long long total = static_cast<long long>(bhn) * p.K * p.P;
   bwd_scan_kernel<Tin><<<dim3(static_cast<unsigned>((total + kThreads - 1) / kThreads), 2), kThreads, 0, s>>>(p, total);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  k3<<<nblk, kThreads, sm3, s>>>(p);
+  k3<<<nblk, kThreadsChunk, sm3, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -1152,11 +1258,23 @@ cudaError_t launch_bwd(const BackwardArgs& a, cudaStream_t s) {
   // 16-byte copies and vector loads: row lengths of 16 bytes' multiples, aligned operands
   const bool vec = d.N % 16 == 0 && d.P % 8 == 0 && p.M % 4 == 0 && aligned16(a.x) && aligned16(a.B) &&
                    aligned16(a.C) && aligned16(a.theta) && aligned16(a.dy);
-  e = vec ? launch_chunk_kernels<Tin, Tdy, true>(p, bhn, s) : launch_chunk_kernels<Tin, Tdy, false>(p, bhn, s);
+  // shapes with kernels specialised at compile time: SISO N 128 P 64 and MIMO rank 4 N 64 P 64
+  if (vec && d.N == 128 && d.P == 64 && d.R == 1 && w.c == 32)
+    e = launch_chunk_kernels<Tin, Tdy, true, 128, 64, 1, 32>(p, bhn, s);
+  else if (vec && d.N == 64 && d.P == 64 && d.R == 4 && w.c == 16)
+    e = launch_chunk_kernels<Tin, Tdy, true, 64, 64, 4, 16>(p, bhn, s);
+  else if (vec)
+    e = launch_chunk_kernels<Tin, Tdy, true, 0, 0, 0, 0>(p, bhn, s);
+  else
+    e = launch_chunk_kernels<Tin, Tdy, false, 0, 0, 0, 0>(p, bhn, s);
   if (e != cudaSuccess) return e;
   bwd_carry_kernel<Tin><<<static_cast<unsigned>(bhn), kThreads, 0, s>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bwd_apply_kernel<Tin><<<static_cast<unsigned>(bhn * w.nch), kThreads, 0, s>>>(p);
+  const int KQ = p.K / 4;
+  if (p.K % 4 == 0 && KQ <= 32 && (32 % KQ) == 0)
+    bwd_apply_kernel<Tin, true><<<static_cast<unsigned>(bhn * w.nch), kThreads, 0, s>>>(p);
+  else
+    bwd_apply_kernel<Tin, false><<<static_cast<unsigned>(bhn * w.nch), kThreads, 0, s>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   dA_reduce_kernel<<<(d.H + 127) / 128, 128, 0, s>>>(p.dApart, a.dA, d.B, d.H);
   return cudaGetLastError();
