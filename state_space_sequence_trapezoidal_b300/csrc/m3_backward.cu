@@ -62,6 +62,7 @@ __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float
 constexpr int kThreads = 256;       // threads of the local, carry and apply kernels
 constexpr int kThreadsChunk = 512;  // threads of the adjoint kernel
 constexpr int kPad = 4;        // floats of padding at the end of each shared-memory row
+constexpr int kPadT = 8;       // the same for rows read only across (the local kernel's inputs)
 constexpr int kMaxRows = 64;   // (token, rank) rows per chunk at most
 constexpr int kMaxTok = 32;    // tokens per chunk at most (one warp lane each)
 
@@ -128,37 +129,18 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// n consecutive floats of shared memory into registers (n = 1, 2 or 4; p aligned to 4 n bytes)
-template <int n>
-__device__ __forceinline__ void ldv(const float* p, float* d) {
-  if constexpr (n == 4) {
-    const float4 q = *reinterpret_cast<const float4*>(p);
-    d[0] = q.x, d[1] = q.y, d[2] = q.z, d[3] = q.w;
-  } else if constexpr (n == 2) {
-    const float2 q = *reinterpret_cast<const float2*>(p);
-    d[0] = q.x, d[1] = q.y;
-  } else {
-    d[0] = p[0];
-  }
-}
-
-// Register-tiled product over the CTA's warps: out(i, j, sum_k A(i, k) B(k, j)) for i < NI,
-// j < NJ.  A(i, k) = a[i * lda + k] when kAK (k contiguous), else a[k * lda + i];
-// B(k, j) = b[j * ldb + k] when kBK, else b[k * ldb + j].  A warp computes a (4 TI) x (8 TJ)
-// tile; lane (gi, gj) = (lane / 8, lane % 8) owns TI of its rows and TJ of its columns.  Along
-// a k-contiguous operand the lane's indices are interleaved (gi + 4 u, gj + 8 v), so that the
-// 4 (8) rows one load instruction touches fall in distinct banks for row strides of 4 (mod 32)
-// words; along an index-contiguous operand they are TI (TJ) consecutive indices read as one
-// vector.  kV: NK and the row strides are multiples of 4, the operands 16-byte aligned and
-// NI % TI == NJ % TJ == 0, and k advances four at a time with 16-byte loads along k;
-// otherwise one k at a time with scalar loads and interleaved indices in both operands.
-// Reads past NI / NJ are clamped to valid rows / columns and their results dropped.  Warp
-// tiles continue the round-robin of the previous product through rr, so that products
-// issued back to back without a barrier share the warps evenly.
-template <int TI, int TJ, bool kAK, bool kBK, bool kV, typename FO>
+// Register-tiled product on the CUDA cores, for the shapes the tensor-core product below does
+// not take: out(i, j, sum_k A(i, k) B(k, j)) for i < NI, j < NJ, with A(i, k) = a[i * lda + k]
+// when kAK (k contiguous), else a[k * lda + i], and B(k, j) = b[j * ldb + k] when kBK, else
+// b[k * ldb + j].  A warp computes a (4 TI) x (8 TJ) tile; lane (gi, gj) = (lane / 8, lane % 8)
+// owns rows gi + 4 u and columns gj + 8 v of it, so that the rows one load instruction touches
+// fall in distinct banks for row strides of 4 (mod 32) words.  Reads past NI / NJ are clamped
+// to valid rows / columns and their results dropped.  Warp tiles continue the round-robin of
+// the previous product through rr, so that products issued back to back without a barrier
+// share the warps evenly.
+template <int TI, int TJ, bool kAK, bool kBK, typename FO>
 __device__ __forceinline__ void gemm(int& rr, int NI, int NJ, int NK, const float* __restrict__ a,
                                      int lda, const float* __restrict__ b, int ldb, FO out) {
-  constexpr bool kBlkI = kV && !kAK, kBlkJ = kV && !kBK;
   constexpr int WI = 4 * TI, WJ = 8 * TJ;
   const int lane = threadIdx.x & 31, nw = static_cast<int>(blockDim.x >> 5);
   const int gi = lane >> 3, gj = lane & 7;
@@ -169,71 +151,32 @@ __device__ __forceinline__ void gemm(int& rr, int NI, int NJ, int NK, const floa
   for (int t = w; t < ntile; t += nw) {
     const int wi = (t / nwj) * WI, wj = (t % nwj) * WJ;
     int ri[TI], rc[TI], cj[TJ], cc[TJ];
-    const int bi = kBlkI ? min(wi + gi * TI, NI - TI) : 0;
-    const int bj = kBlkJ ? min(wj + gj * TJ, NJ - TJ) : 0;
 #pragma unroll
     for (int u = 0; u < TI; ++u) {
-      ri[u] = kBlkI ? wi + gi * TI + u : wi + gi + 4 * u;
-      rc[u] = kBlkI ? bi + u : min(ri[u], NI - 1);
+      ri[u] = wi + gi + 4 * u;
+      rc[u] = min(ri[u], NI - 1);
     }
 #pragma unroll
     for (int v = 0; v < TJ; ++v) {
-      cj[v] = kBlkJ ? wj + gj * TJ + v : wj + gj + 8 * v;
-      cc[v] = kBlkJ ? bj + v : min(cj[v], NJ - 1);
+      cj[v] = wj + gj + 8 * v;
+      cc[v] = min(cj[v], NJ - 1);
     }
     float acc[TI][TJ];
 #pragma unroll
     for (int u = 0; u < TI; ++u)
 #pragma unroll
       for (int v = 0; v < TJ; ++v) acc[u][v] = 0.f;
-    if constexpr (kV) {
-#pragma unroll 4
-      for (int k0 = 0; k0 < NK; k0 += 4) {
-        float av[4][TI], bv[4][TJ];
-        if constexpr (kAK) {
-#pragma unroll
-          for (int u = 0; u < TI; ++u) {
-            float q[4];
-            ldv<4>(a + rc[u] * lda + k0, q);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) av[kk][u] = q[kk];
-          }
-        } else {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) ldv<TI>(a + (k0 + kk) * lda + bi, av[kk]);
-        }
-        if constexpr (kBK) {
-#pragma unroll
-          for (int v = 0; v < TJ; ++v) {
-            float q[4];
-            ldv<4>(b + cc[v] * ldb + k0, q);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) bv[kk][v] = q[kk];
-          }
-        } else {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) ldv<TJ>(b + (k0 + kk) * ldb + bj, bv[kk]);
-        }
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-          for (int u = 0; u < TI; ++u)
-#pragma unroll
-            for (int v = 0; v < TJ; ++v) acc[u][v] = fmaf(av[kk][u], bv[kk][v], acc[u][v]);
-      }
-    } else {
 #pragma unroll 2
-      for (int k = 0; k < NK; ++k) {
-        float av[TI], bv[TJ];
+    for (int k = 0; k < NK; ++k) {
+      float av[TI], bv[TJ];
 #pragma unroll
-        for (int u = 0; u < TI; ++u) av[u] = kAK ? a[rc[u] * lda + k] : a[k * lda + rc[u]];
+      for (int u = 0; u < TI; ++u) av[u] = kAK ? a[rc[u] * lda + k] : a[k * lda + rc[u]];
 #pragma unroll
-        for (int v = 0; v < TJ; ++v) bv[v] = kBK ? b[cc[v] * ldb + k] : b[k * ldb + cc[v]];
+      for (int v = 0; v < TJ; ++v) bv[v] = kBK ? b[cc[v] * ldb + k] : b[k * ldb + cc[v]];
 #pragma unroll
-        for (int u = 0; u < TI; ++u)
+      for (int u = 0; u < TI; ++u)
 #pragma unroll
-          for (int v = 0; v < TJ; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
-      }
+        for (int v = 0; v < TJ; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
     }
 #pragma unroll
     for (int u = 0; u < TI; ++u)
@@ -241,6 +184,110 @@ __device__ __forceinline__ void gemm(int& rr, int NI, int NJ, int NK, const floa
       for (int v = 0; v < TJ; ++v)
         if (ri[u] < NI && cj[v] < NJ) out(ri[u], cj[v], acc[u][v]);
   }
+}
+
+// ------------------------------------------------------------------ tensor-core products
+// fp32 values as TF32 pairs: x = hi + lo with hi = x rounded to TF32 and lo the rest rounded
+// again; a product taken as a_lo b_hi + a_hi b_lo + a_hi b_hi (the lo lo term dropped) keeps
+// about 21 bits of each operand, the accuracy of an fp32 dot product for these sizes.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  hi = to_tf32(x);
+  lo = to_tf32(x - __uint_as_float(hi));
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// The product of gemm() on the tensor cores: warp-level m16n8k8 TF32 MMAs in three passes per
+// fragment pair (split_tf32), accumulators in fp32 registers.  A warp computes a (16 MI) x
+// (8 NJ) tile; fragments are read from shared memory with 32-bit loads in the MMA's register
+// layout (lane = 4 g + t: A rows g, g + 8, k t, t + 4; B k t, t + 4, column g; D rows g, g + 8,
+// columns 2 t, 2 t + 1).  With row strides of 4 (mod 32) words the loads along a k-contiguous
+// operand are free of bank conflicts (4 g + t); along an index-contiguous one two lanes share
+// a bank.  Needs NI % 16 == 0, NJ % 8 == 0 and NK % 8 == 0 (fragments wholly in or out); the
+// in / out tests are the same for all lanes of a warp, as mma.sync requires.
+template <int MI, int NJ, bool kAK, bool kBK, typename FO>
+__device__ __forceinline__ void gemm_tc(int& rr, int NI, int NJd, int NK, const float* __restrict__ a,
+                                        int lda, const float* __restrict__ b, int ldb, FO out) {
+  constexpr int WI = 16 * MI, WJ = 8 * NJ;
+  const int lane = threadIdx.x & 31, nw = static_cast<int>(blockDim.x >> 5);
+  const int g = lane >> 2, t = lane & 3;
+  const int nwj = (NJd + WJ - 1) / WJ, ntile = ((NI + WI - 1) / WI) * nwj;
+  int w = static_cast<int>(threadIdx.x >> 5) - rr % nw;
+  if (w < 0) w += nw;
+  rr += ntile;
+  auto A = [&](int i, int k) { return kAK ? a[i * lda + k] : a[k * lda + i]; };
+  auto B = [&](int k, int j) { return kBK ? b[j * ldb + k] : b[k * ldb + j]; };
+  for (int tile = w; tile < ntile; tile += nw) {
+    const int i0 = (tile / nwj) * WI, j0 = (tile % nwj) * WJ;
+    float acc[MI][NJ][4];
+#pragma unroll
+    for (int mi = 0; mi < MI; ++mi)
+#pragma unroll
+      for (int nj = 0; nj < NJ; ++nj) acc[mi][nj][0] = acc[mi][nj][1] = acc[mi][nj][2] = acc[mi][nj][3] = 0.f;
+#pragma unroll 2
+    for (int k0 = 0; k0 < NK; k0 += 8) {
+      uint32_t ah[MI][4], al[MI][4], bh[NJ][2], bl[NJ][2];
+#pragma unroll
+      for (int mi = 0; mi < MI; ++mi) {
+        if (i0 + 16 * mi < NI) {
+          const int r0 = i0 + 16 * mi + g;
+          split_tf32(A(r0, k0 + t), ah[mi][0], al[mi][0]);
+          split_tf32(A(r0 + 8, k0 + t), ah[mi][1], al[mi][1]);
+          split_tf32(A(r0, k0 + t + 4), ah[mi][2], al[mi][2]);
+          split_tf32(A(r0 + 8, k0 + t + 4), ah[mi][3], al[mi][3]);
+        }
+      }
+#pragma unroll
+      for (int nj = 0; nj < NJ; ++nj) {
+        if (j0 + 8 * nj < NJd) {
+          const int c = j0 + 8 * nj + g;
+          split_tf32(B(k0 + t, c), bh[nj][0], bl[nj][0]);
+          split_tf32(B(k0 + t + 4, c), bh[nj][1], bl[nj][1]);
+        }
+      }
+#pragma unroll
+      for (int mi = 0; mi < MI; ++mi)
+#pragma unroll
+        for (int nj = 0; nj < NJ; ++nj)
+          if (i0 + 16 * mi < NI && j0 + 8 * nj < NJd) {
+            mma_tf32(acc[mi][nj], al[mi], bh[nj]);
+            mma_tf32(acc[mi][nj], ah[mi], bl[nj]);
+            mma_tf32(acc[mi][nj], ah[mi], bh[nj]);
+          }
+    }
+#pragma unroll
+    for (int mi = 0; mi < MI; ++mi)
+#pragma unroll
+      for (int nj = 0; nj < NJ; ++nj)
+        if (i0 + 16 * mi < NI && j0 + 8 * nj < NJd) {
+          const int r0 = i0 + 16 * mi + g, c0 = j0 + 8 * nj + 2 * t;
+          out(r0, c0, acc[mi][nj][0]);
+          out(r0, c0 + 1, acc[mi][nj][1]);
+          out(r0 + 8, c0, acc[mi][nj][2]);
+          out(r0 + 8, c0 + 1, acc[mi][nj][3]);
+        }
+  }
+}
+
+// The product on the tensor cores where the shapes allow (kV: N % 16, P % 8 and the row count
+// M % 16 all zero, operands 16-byte aligned), else on the CUDA cores.
+template <int MI, int NJ, int TI, int TJ, bool kAK, bool kBK, bool kV, typename FO>
+__device__ __forceinline__ void product(int& rr, int NI, int NJd, int NK, const float* __restrict__ a,
+                                        int lda, const float* __restrict__ b, int ldb, FO out) {
+  if constexpr (kV)
+    gemm_tc<MI, NJ, kAK, kBK>(rr, NI, NJd, NK, a, lda, b, ldb, out);
+  else
+    gemm<TI, TJ, kAK, kBK>(rr, NI, NJd, NK, a, lda, b, ldb, out);
 }
 
 // Fixed-order sum over the CTA of one float per thread (scratch: blockDim.x floats).
@@ -277,7 +324,8 @@ __host__ __device__ inline int raw_floats(int M, int len, int sz) {
 
 // Per-chunk inputs shared by the local and adjoint kernels.
 struct InSmem {
-  int Bt, Ct, X, dY;               // fp32 rows [M][N + kPad] / [M][P + kPad]
+  int ldN, ldP;                    // row strides of the fp32 rows: N + pad, P + pad
+  int Bt, Ct, X, dY;               // fp32 rows [M][ldN] / [M][ldP]
   int rB, rC, rX, rY;              // raw staging of 16-bit inputs
   int th, cs, sn;                  // theta as loaded, cos / sin of psi [c][K]
   int dt, lam, ell, el, gam, q;    // per token (q: c + 1, the next chunk's first token last)
@@ -285,12 +333,14 @@ struct InSmem {
   int part;                        // scratch of the angle pass
 };
 __host__ __device__ inline void carve_inputs(Carve& cv, InSmem& s, int N, int P, int R, int c, int szIn,
-                                             int szDy, int raw_at) {
+                                             int szDy, int raw_at, int pad) {
   const int K = N / 2, M = c * R;
-  s.Bt = cv.take(M * (N + kPad));
-  s.Ct = cv.take(M * (N + kPad));
-  s.X = cv.take(M * (P + kPad));
-  s.dY = cv.take(M * (P + kPad));
+  s.ldN = N + pad;
+  s.ldP = P + pad;
+  s.Bt = cv.take(M * s.ldN);
+  s.Ct = cv.take(M * s.ldN);
+  s.X = cv.take(M * s.ldP);
+  s.dY = cv.take(M * s.ldP);
   s.th = cv.take((c * K * szIn + 3) / 4);
   s.cs = cv.take(c * K);
   s.sn = cv.take(c * K);
@@ -325,7 +375,7 @@ struct LocalSmem {
 __host__ __device__ inline LocalSmem local_smem(int N, int P, int R, int c, int szIn, int szDy) {
   LocalSmem s{};
   Carve cv;
-  carve_inputs(cv, s.in, N, P, R, c, szIn, szDy, -1);
+  carve_inputs(cv, s.in, N, P, R, c, szIn, szDy, -1, kPadT);
   s.total = cv.o;
   return s;
 }
@@ -342,7 +392,7 @@ __host__ __device__ inline ChunkSmem chunk_smem(int N, int P, int R, int c, int 
   s.XG = cv.take(M * (N + kPad));  // X Gout^T, then dB~
   // the raw inputs wait in Q and XG when they fit there (both are written after conversion)
   const int raw = raw_total(N, P, R, c, szIn, szDy);
-  carve_inputs(cv, s.in, N, P, R, c, szIn, szDy, raw <= 2 * M * (N + kPad) ? s.Q : -1);
+  carve_inputs(cv, s.in, N, P, R, c, szIn, szDy, raw <= 2 * M * (N + kPad) ? s.Q : -1, kPad);
   s.W = cv.take(M * (P + kPad));   // B~ Gout
   s.Hp = cv.take(N * (P + kPad));
   s.Go = cv.take(N * (P + kPad));
@@ -579,13 +629,13 @@ __device__ __forceinline__ void load_chunk(const BwdParams& p, const Shape& sh, 
   const size_t ts = p.H;
   issue_theta<Tin, kV>(p, sh, q, sm + L.th);
   if constexpr (kV) cp_async_commit();
-  issue_rows<Tin, kV>(static_cast<const Tin*>(p.B), q, ts, c, R, N, sm + L.Bt, N + kPad,
+  issue_rows<Tin, kV>(static_cast<const Tin*>(p.B), q, ts, c, R, N, sm + L.Bt, L.ldN,
                       reinterpret_cast<Tin*>(sm + L.rB));
-  issue_rows<Tin, kV>(static_cast<const Tin*>(p.C), q, ts, c, R, N, sm + L.Ct, N + kPad,
+  issue_rows<Tin, kV>(static_cast<const Tin*>(p.C), q, ts, c, R, N, sm + L.Ct, L.ldN,
                       reinterpret_cast<Tin*>(sm + L.rC));
-  issue_rows<Tin, kV>(static_cast<const Tin*>(p.x), q, ts, c, R, P, sm + L.X, P + kPad,
+  issue_rows<Tin, kV>(static_cast<const Tin*>(p.x), q, ts, c, R, P, sm + L.X, L.ldP,
                       reinterpret_cast<Tin*>(sm + L.rX));
-  issue_rows<Tdy, kV>(static_cast<const Tdy*>(p.dy), q, ts, c, R, P, sm + L.dY, P + kPad,
+  issue_rows<Tdy, kV>(static_cast<const Tdy*>(p.dy), q, ts, c, R, P, sm + L.dY, L.ldP,
                       reinterpret_cast<Tdy*>(sm + L.rY));
   extra();
   if constexpr (kV) cp_async_commit();
@@ -596,13 +646,13 @@ __device__ __forceinline__ void load_chunk(const BwdParams& p, const Shape& sh, 
   scales();  // per-row weights from the coefficients
   if constexpr (kV) cp_async_wait_all();
   __syncthreads();
-  finish_rows<Tin, kV>(q, c, R, N, sm + L.Bt, N + kPad, reinterpret_cast<const Tin*>(sm + L.rB), true,
+  finish_rows<Tin, kV>(q, c, R, N, sm + L.Bt, L.ldN, reinterpret_cast<const Tin*>(sm + L.rB), true,
                        sm + L.cs, sm + L.sn, K, nullptr);
-  finish_rows<Tin, kV>(q, c, R, N, sm + L.Ct, N + kPad, reinterpret_cast<const Tin*>(sm + L.rC), true,
+  finish_rows<Tin, kV>(q, c, R, N, sm + L.Ct, L.ldN, reinterpret_cast<const Tin*>(sm + L.rC), true,
                        sm + L.cs, sm + L.sn, K, nullptr);
-  finish_rows<Tin, kV>(q, c, R, P, sm + L.X, P + kPad, reinterpret_cast<const Tin*>(sm + L.rX), false,
+  finish_rows<Tin, kV>(q, c, R, P, sm + L.X, L.ldP, reinterpret_cast<const Tin*>(sm + L.rX), false,
                        nullptr, nullptr, K, scale_x ? sm + L.wx : nullptr);
-  finish_rows<Tdy, kV>(q, c, R, P, sm + L.dY, P + kPad, reinterpret_cast<const Tdy*>(sm + L.rY), false,
+  finish_rows<Tdy, kV>(q, c, R, P, sm + L.dY, L.ldP, reinterpret_cast<const Tdy*>(sm + L.rY), false,
                        nullptr, nullptr, K, scale_y ? sm + L.rowel : nullptr);
   __syncthreads();
 }
@@ -640,9 +690,9 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_local_kernel(const BwdParams 
   float* dH = p.wsH + slot * N * P;
   float* dG = p.wsG + slot * N * P;
   int rr = 0;
-  gemm<4, 4, false, false, kV>(rr, N, P, M, sm + L.Bt, N + kPad, sm + L.X, P + kPad,
+  product<2, 4, 4, 4, false, false, kV>(rr, N, P, M, sm + L.Bt, L.ldN, sm + L.X, L.ldP,
                                [&](int n, int pc, float v) { dH[n * P + pc] = v; });
-  gemm<4, 4, false, false, kV>(rr, N, P, M, sm + L.Ct, N + kPad, sm + L.dY, P + kPad,
+  product<2, 4, 4, 4, false, false, kV>(rr, N, P, M, sm + L.Ct, L.ldN, sm + L.dY, L.ldP,
                                [&](int n, int pc, float v) { dG[n * P + pc] = v; });
 }
 
@@ -761,7 +811,7 @@ __global__ void __launch_bounds__(kThreadsChunk, 1) bwd_chunk_kernel(const BwdPa
   const int N = sh.N, P = sh.P, R = sh.R, c = sh.c, M = sh.M, K = sh.K, NP = N * P;
   const int bh = blockIdx.x / p.nch, k = blockIdx.x % p.nch;
   const ChunkPos q = chunk_pos(p, bh, k, c);
-  const int ldN = N + kPad, ldP = P + kPad, ldM = M + kPad, ldT = c + 1;
+  const int ldN = N + kPad, ldP = P + kPad, ldM = M + kPad, ldT = c + 1;  // = L.ldN, L.ldP
   const ChunkSmem S = chunk_smem(N, P, R, c, sizeof(Tin), sizeof(Tdy));
   const InSmem& L = S.in;
   const size_t slot = static_cast<size_t>(bh) * p.nch + k;
@@ -846,15 +896,15 @@ __global__ void __launch_bounds__(kThreadsChunk, 1) bwd_chunk_kernel(const BwdPa
   int rr = 0;
   // W = B~ Gout, S = C~ B~^T, Q = dY Hp^T, XG = X Gout^T, E = dY X^T (tiles of about equal
   // work, the largest products first)
-  gemm<2, 4, true, false, kV>(rr, M, P, N, sBt, ldN, sGo, ldP,
+  product<2, 2, 2, 4, true, false, kV>(rr, M, P, N, sBt, ldN, sGo, ldP,
                               [&](int s_, int pc, float v) { sW[s_ * ldP + pc] = v; });
-  gemm<2, 4, true, true, kV>(rr, M, M, N, sCt, ldN, sBt, ldN,
+  product<2, 2, 2, 4, true, true, kV>(rr, M, M, N, sCt, ldN, sBt, ldN,
                              [&](int i, int s_, float v) { sS[i * ldM + s_] = v; });
-  gemm<4, 4, true, true, kV>(rr, M, N, P, sdY, ldP, sHp, ldP,
+  product<2, 2, 4, 4, true, true, kV>(rr, M, N, P, sdY, ldP, sHp, ldP,
                              [&](int i, int n, float v) { sQ[i * ldN + n] = v; });
-  gemm<4, 4, true, true, kV>(rr, M, N, P, sX, ldP, sGo, ldP,
+  product<2, 2, 4, 4, true, true, kV>(rr, M, N, P, sX, ldP, sGo, ldP,
                              [&](int s_, int n, float v) { sXG[s_ * ldN + n] = v; });
-  gemm<2, 4, true, true, kV>(rr, M, M, P, sdY, ldP, sX, ldP,
+  product<2, 2, 2, 4, true, true, kV>(rr, M, M, P, sdY, ldP, sX, ldP,
                              [&](int i, int s_, float v) { sE[i * ldM + s_] = v; });
   __syncthreads();
 
@@ -905,16 +955,16 @@ __global__ void __launch_bounds__(kThreadsChunk, 1) bwd_chunk_kernel(const BwdPa
   // ---------------------------------------------------------------- gradients of the rows
   rr = 0;
   // dC~ = (Mh o E) B~ + exp(l) Q, over Q
-  gemm<2, 4, true, false, kV>(rr, M, N, M, sE, ldM, sBt, ldN, [&](int i, int n, float v) {
+  product<2, 2, 2, 4, true, false, kV>(rr, M, N, M, sE, ldM, sBt, ldN, [&](int i, int n, float v) {
     sQ[i * ldN + n] = fmaf(s_rowel[i], sQ[i * ldN + n], v);
   });
   // dB~ = (Mh o E)^T C~ + wx X Gout^T, over XG
-  gemm<2, 4, false, false, kV>(rr, M, N, M, sE, ldM, sCt, ldN, [&](int s_, int n, float v) {
+  product<2, 2, 2, 4, false, false, kV>(rr, M, N, M, sE, ldM, sCt, ldN, [&](int s_, int n, float v) {
     sXG[s_ * ldN + n] = fmaf(s_wx[s_], sXG[s_ * ldN + n], v);
   });
   // dX = (Mh o S)^T dY + wx W, to global
   float* dxg = p.dx;
-  gemm<2, 4, false, false, kV>(rr, M, P, M, sS, ldM, sdY, ldP, [&](int s_, int pc, float v) {
+  product<2, 2, 2, 4, false, false, kV>(rr, M, P, M, sS, ldM, sdY, ldP, [&](int s_, int pc, float v) {
     const int ts = s_ / R;
     if (ts < q.nt)
       dxg[(q.tok0 + static_cast<size_t>(ts) * tstride) * R * P + static_cast<size_t>(s_ - ts * R) * P + pc] =
@@ -1255,8 +1305,9 @@ cudaError_t launch_bwd(const BackwardArgs& a, cudaStream_t s) {
   p.M = w.c * d.R;
   p.nch = w.nch;
   p.K = d.N / 2;
-  // 16-byte copies and vector loads: row lengths of 16 bytes' multiples, aligned operands
-  const bool vec = d.N % 16 == 0 && d.P % 8 == 0 && p.M % 4 == 0 && aligned16(a.x) && aligned16(a.B) &&
+  // 16-byte copies and tensor-core products: row lengths of 16 bytes' multiples, aligned operands,
+  // (token, rank) rows a multiple of 16
+  const bool vec = d.N % 16 == 0 && d.P % 8 == 0 && p.M % 16 == 0 && aligned16(a.x) && aligned16(a.B) &&
                    aligned16(a.C) && aligned16(a.theta) && aligned16(a.dy);
   // shapes with kernels specialised at compile time: SISO N 128 P 64 and MIMO rank 4 N 64 P 64
   if (vec && d.N == 128 && d.P == 64 && d.R == 1 && w.c == 32)
