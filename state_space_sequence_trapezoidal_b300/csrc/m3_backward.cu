@@ -97,6 +97,7 @@ struct BwdParams {
   float* wsDqf;   // [BH][nch]       d q of chunk k's first token through the fold
   float* dApart;  // [BH]
   int T, H, N, P, R, c, M, nch, K;
+  int BH;  // sequences (batch rows x heads)
 };
 
 __device__ __forceinline__ float wrap(float a) {
@@ -333,7 +334,7 @@ struct InSmem {
   int part;                        // scratch of the angle pass
 };
 __host__ __device__ inline void carve_inputs(Carve& cv, InSmem& s, int N, int P, int R, int c, int szIn,
-                                             int szDy, int raw_at, int pad) {
+                                             int szDy, int raw_at, int pad, bool theta_here = true) {
   const int K = N / 2, M = c * R;
   s.ldN = N + pad;
   s.ldP = P + pad;
@@ -341,7 +342,7 @@ __host__ __device__ inline void carve_inputs(Carve& cv, InSmem& s, int N, int P,
   s.Ct = cv.take(M * s.ldN);
   s.X = cv.take(M * s.ldP);
   s.dY = cv.take(M * s.ldP);
-  s.th = cv.take((c * K * szIn + 3) / 4);
+  s.th = theta_here ? cv.take((c * K * szIn + 3) / 4) : -1;
   s.cs = cv.take(c * K);
   s.sn = cv.take(c * K);
   s.dt = cv.take(c);
@@ -382,7 +383,7 @@ __host__ __device__ inline LocalSmem local_smem(int N, int P, int R, int c, int 
 
 struct ChunkSmem {
   InSmem in;
-  int Q, XG, W, Hp, Go, S, E, dphi, Mh, ex, dM, dexp, wdot, dell, dgam, dq, red, total;
+  int Q, XG, W, Hp, Go, S, E, th, dphi, Mh, ex, dM, dexp, wdot, dell, dgam, dq, red, total;
 };
 __host__ __device__ inline ChunkSmem chunk_smem(int N, int P, int R, int c, int szIn, int szDy) {
   const int K = N / 2, M = c * R;
@@ -392,14 +393,14 @@ __host__ __device__ inline ChunkSmem chunk_smem(int N, int P, int R, int c, int 
   s.XG = cv.take(M * (N + kPad));  // X Gout^T, then dB~
   // the raw inputs wait in Q and XG when they fit there (both are written after conversion)
   const int raw = raw_total(N, P, R, c, szIn, szDy);
-  carve_inputs(cv, s.in, N, P, R, c, szIn, szDy, raw <= 2 * M * (N + kPad) ? s.Q : -1, kPad);
-  s.W = cv.take(M * (P + kPad));   // B~ Gout
-  s.Hp = cv.take(N * (P + kPad));
-  s.Go = cv.take(N * (P + kPad));
-  s.S = cv.take(M * (M + kPad));   // C~ B~^T, then Mh o S
+  carve_inputs(cv, s.in, N, P, R, c, szIn, szDy, raw <= 2 * M * (N + kPad) ? s.Q : -1, kPad, false);
+  s.W = cv.take(M * (P + kPad));   // B~ Gout; then d phi per (token, pair), where it fits
+  s.Hp = cv.take(N * (P + kPad));  // Hp; the next chunk's from the end of the first products
+  s.Go = cv.take(N * (P + kPad));  // Gout, likewise
+  s.S = cv.take(M * (M + kPad));   // C~ B~^T, then Mh o S; then the next chunk's theta
   s.E = cv.take(M * (M + kPad));   // dY X^T, then Mh o E
-  // d phi per (token, pair) takes Hp's place (Hp is last read by the state products)
-  s.dphi = c * K <= N * (P + kPad) ? s.Hp : cv.take(c * K);
+  s.th = c * K <= 2 * M * (M + kPad) ? s.S : cv.take(c * K);  // theta, fp32 or raw 16-bit
+  s.dphi = c * K <= M * (P + kPad) ? s.W : cv.take(c * K);
   s.Mh = cv.take(c * (c + 1));
   s.ex = cv.take(c * (c + 1));
   s.dM = cv.take(c * (c + 1));
@@ -515,28 +516,43 @@ __device__ __forceinline__ void finish_rows(const ChunkPos& q, int c, int R, int
 
 // Per-token coefficients (warp 0, one lane per token, tokens >= nt zero): dt, lambda, the
 // chunk-local log-decay sums l, exp(l), gamma, q, and q of the next chunk's first token.
+// dt and lambda of the chunk's tokens (lane t of warp 0; zero past nt), of the next chunk's first
+// token (lane 0), and the head's A (warp 0), for chunk_coefs.
+struct CoefIn {
+  float dt, lam, dtn, lamn, A;
+};
 template <typename Tin>
-__device__ __forceinline__ void chunk_coefs(const BwdParams& p, const Shape& sh, const ChunkPos& q, float A,
-                                            const InSmem& L, float* sm) {
+__device__ __forceinline__ CoefIn load_coefs(const BwdParams& p, const ChunkPos& q) {
+  CoefIn v{0.f, 0.f, 0.f, 0.f, 0.f};
   if (threadIdx.x < 32) {
+    v.A = p.A[(q.tok0 % p.H)];
     const Tin* dtg = static_cast<const Tin*>(p.dt);
     const Tin* lamg = static_cast<const Tin*>(p.lam);
     const int t = threadIdx.x;
-    const bool ok = t < q.nt;
-    const size_t o = q.tok0 + static_cast<size_t>(t) * p.H;
-    const float dt = ok ? to_f(dtg[o]) : 0.f;
-    const float lam = ok ? to_f(lamg[o]) : 0.f;
-    float dtn = 0.f, lamn = 0.f;  // the next chunk's first token, loaded with the others
+    if (t < q.nt) {
+      const size_t o = q.tok0 + static_cast<size_t>(t) * p.H;
+      v.dt = to_f(dtg[o]);
+      v.lam = to_f(lamg[o]);
+    }
     if (t == 0 && q.has_next) {
       const size_t tn = q.tok0 + static_cast<size_t>(q.nt) * p.H;
-      dtn = to_f(dtg[tn]);
-      lamn = to_f(lamg[tn]);
+      v.dtn = to_f(dtg[tn]);
+      v.lamn = to_f(lamg[tn]);
     }
+  }
+  return v;
+}
+__device__ __forceinline__ void chunk_coefs_from(const Shape& sh, const ChunkPos& q, float A, const InSmem& L,
+                                                 float* sm, const CoefIn& v) {
+  if (threadIdx.x < 32) {
+    const int t = threadIdx.x;
+    const bool ok = t < q.nt;
+    const float dt = v.dt, lam = v.lam, dtn = v.dtn, lamn = v.lamn;
     float ell = dt * A;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-      const float v = __shfl_up_sync(0xffffffffu, ell, d);
-      if (t >= d) ell += v;
+      const float u = __shfl_up_sync(0xffffffffu, ell, d);
+      if (t >= d) ell += u;
     }
     if (t < sh.c) {
       sm[L.dt + t] = dt;
@@ -548,6 +564,11 @@ __device__ __forceinline__ void chunk_coefs(const BwdParams& p, const Shape& sh,
     }
     if (t == 0) sm[L.q + sh.c] = (1.f - lamn) * dtn;
   }
+}
+template <typename Tin>
+__device__ __forceinline__ void chunk_coefs(const BwdParams& p, const Shape& sh, const ChunkPos& q, float A,
+                                            const InSmem& L, float* sm) {
+  chunk_coefs_from(sh, q, A, L, sm, load_coefs<Tin>(p, q));
 }
 
 // theta rows of the chunk into the th area (asynchronous copies when kV, else fp32 scalars).
@@ -586,9 +607,8 @@ __device__ __forceinline__ float theta_at(const float* s_th, int e) {
 // the CTA calls it.
 template <typename Tin, bool kV>
 __device__ __forceinline__ void chunk_angles(const ChunkPos& q, const Shape& sh, float* sm, const InSmem& L,
-                                             float* sig_out) {
+                                             const float* s_th, float* sig_out) {
   const int K = sh.K, c = sh.c, nthr = blockDim.x;
-  const float* s_th = sm + L.th;
   float* s_part = sm + L.part;
   float* s_cs = sm + L.cs;
   float* s_sn = sm + L.sn;
@@ -642,7 +662,7 @@ __device__ __forceinline__ void load_chunk(const BwdParams& p, const Shape& sh, 
   chunk_coefs<Tin>(p, sh, q, A, L, sm);
   if constexpr (kV) asm volatile("cp.async.wait_group 1;" ::: "memory");
   __syncthreads();
-  chunk_angles<Tin, kV>(q, sh, sm, L, sig_out);
+  chunk_angles<Tin, kV>(q, sh, sm, L, sm + L.th, sig_out);
   scales();  // per-row weights from the coefficients
   if constexpr (kV) cp_async_wait_all();
   __syncthreads();
@@ -804,19 +824,16 @@ __global__ void __launch_bounds__(kThreads) bwd_scan_kernel(const BwdParams p, l
 }
 
 // ------------------------------------------------------------------ per-chunk adjoint
-template <typename Tin, typename Tdy, bool kV, int SN, int SP, int SR, int SC>
-__global__ void __launch_bounds__(kThreadsChunk, 1) bwd_chunk_kernel(const BwdParams p) {
+template <typename Tin, typename Tdy, bool kV, int SN, int SP, int SR, int SC, int NT>
+__global__ void __launch_bounds__(NT, 1) bwd_chunk_kernel(const BwdParams p) {
   extern __shared__ __align__(16) float sm[];
   const Shape sh = shape_of<SN, SP, SR, SC>(p);
   const int N = sh.N, P = sh.P, R = sh.R, c = sh.c, M = sh.M, K = sh.K, NP = N * P;
-  const int bh = blockIdx.x / p.nch, k = blockIdx.x % p.nch;
-  const ChunkPos q = chunk_pos(p, bh, k, c);
   const int ldN = N + kPad, ldP = P + kPad, ldM = M + kPad, ldT = c + 1;  // = L.ldN, L.ldP
   const ChunkSmem S = chunk_smem(N, P, R, c, sizeof(Tin), sizeof(Tdy));
   const InSmem& L = S.in;
-  const size_t slot = static_cast<size_t>(bh) * p.nch + k;
   const size_t tstride = p.H;
-  const float A = p.A[bh % p.H];
+  const int total = p.BH * p.nch;
   float* sBt = sm + L.Bt;
   float* sCt = sm + L.Ct;
   float* sX = sm + L.X;
@@ -848,30 +865,63 @@ __global__ void __launch_bounds__(kThreadsChunk, 1) bwd_chunk_kernel(const BwdPa
   const float* s_rowel = sm + L.rowel;
   const float* s_cs = sm + L.cs;
   const float* s_sn = sm + L.sn;
-  const float* hp = p.wsH + slot * NP;
-  const float* go = p.wsG + slot * NP;
+  float* s_th = sm + S.th;
+  const Tin* thg = static_cast<const Tin*>(p.theta);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  // a chunk's Hp and Gout into their areas (asynchronous copies when kV)
+  auto fetch_state = [&](size_t slot_) {
+    const float* hp = p.wsH + slot_ * NP;
+    const float* go = p.wsG + slot_ * NP;
+    if constexpr (kV) {
+      const int per = P / 4;
+      for (int e = threadIdx.x; e < N * per; e += blockDim.x) {
+        const int n = e / per, col = (e - n * per) * 4;
+        cp_async16(sHp + n * ldP + col, hp + n * P + col);
+        cp_async16(sGo + n * ldP + col, go + n * P + col);
+      }
+    } else {
+      for (int e = threadIdx.x; e < NP; e += blockDim.x) {
+        const int n = e / P, col = e - n * P;
+        sHp[n * ldP + col] = hp[e];
+        sGo[n * ldP + col] = go[e];
+      }
+    }
+  };
+  auto pos_of = [&](int j) { return chunk_pos(p, j / p.nch, j % p.nch, c); };
 
-  // ---------------------------------------------------------------- inputs, Hp and Gout
-  load_chunk<Tin, Tdy, kV>(
-      p, sh, q, A, L, sm, nullptr,
-      [&] {
-        if constexpr (kV) {
-          const int per = P / 4;
-          for (int e = threadIdx.x; e < N * per; e += blockDim.x) {
-            const int n = e / per, col = (e - n * per) * 4;
-            cp_async16(sHp + n * ldP + col, hp + n * P + col);
-            cp_async16(sGo + n * ldP + col, go + n * P + col);
-          }
-        } else {
-          for (int e = threadIdx.x; e < NP; e += blockDim.x) {
-            const int n = e / P, col = e - n * P;
-            sHp[n * ldP + col] = hp[e];
-            sGo[n * ldP + col] = go[e];
-          }
-        }
-      },
-      [&] { row_weights(q, c, R, L, sm); }, false, false);
+  // Persistent: CTA b takes chunks b, b + gridDim.x, ...; theta, Hp, Gout, dt and lambda of the
+  // next chunk are requested while the current one finishes (their areas are free by then).
+  CoefIn cin{0.f, 0.f, 0.f, 0.f, 0.f};
+  if (static_cast<int>(blockIdx.x) < total) {
+    const ChunkPos q0 = pos_of(blockIdx.x);
+    issue_theta<Tin, kV>(p, sh, q0, s_th);
+    fetch_state(blockIdx.x);
+    if constexpr (kV) cp_async_commit();
+    cin = load_coefs<Tin>(p, q0);
+  }
+  for (int j = blockIdx.x; j < total; j += gridDim.x) {
+  const ChunkPos q = pos_of(j);
+  const size_t slot = j;
+  const float A = cin.A;  // (warp 0 only: the coefficients and d dt use it)
+
+  // ---------------------------------------------------------------- inputs of the chunk
+  issue_rows<Tin, kV>(static_cast<const Tin*>(p.B), q, tstride, c, R, N, sBt, ldN, reinterpret_cast<Tin*>(sm + L.rB));
+  issue_rows<Tin, kV>(static_cast<const Tin*>(p.C), q, tstride, c, R, N, sCt, ldN, reinterpret_cast<Tin*>(sm + L.rC));
+  issue_rows<Tin, kV>(static_cast<const Tin*>(p.x), q, tstride, c, R, P, sX, ldP, reinterpret_cast<Tin*>(sm + L.rX));
+  issue_rows<Tdy, kV>(static_cast<const Tdy*>(p.dy), q, tstride, c, R, P, sdY, ldP, reinterpret_cast<Tdy*>(sm + L.rY));
+  if constexpr (kV) cp_async_commit();
+  chunk_coefs_from(sh, q, A, L, sm, cin);
+  if constexpr (kV) asm volatile("cp.async.wait_group 1;" ::: "memory");  // theta, Hp, Gout
+  __syncthreads();
+  chunk_angles<Tin, kV>(q, sh, sm, L, s_th, nullptr);
+  row_weights(q, c, R, L, sm);
+  if constexpr (kV) cp_async_wait_all();
+  __syncthreads();
+  finish_rows<Tin, kV>(q, c, R, N, sBt, ldN, reinterpret_cast<const Tin*>(sm + L.rB), true, s_cs, s_sn, K, nullptr);
+  finish_rows<Tin, kV>(q, c, R, N, sCt, ldN, reinterpret_cast<const Tin*>(sm + L.rC), true, s_cs, s_sn, K, nullptr);
+  finish_rows<Tin, kV>(q, c, R, P, sX, ldP, reinterpret_cast<const Tin*>(sm + L.rX), false, nullptr, nullptr, K, nullptr);
+  finish_rows<Tdy, kV>(q, c, R, P, sdY, ldP, reinterpret_cast<const Tdy*>(sm + L.rY), false, nullptr, nullptr, K, nullptr);
+  __syncthreads();
 
   // ---------------------------------------------------------------- products with the inputs
   // tables per token pair: exp(l_i - l_s) and Mh[i, s]
@@ -907,6 +957,14 @@ __global__ void __launch_bounds__(kThreadsChunk, 1) bwd_chunk_kernel(const BwdPa
   product<2, 2, 2, 4, true, true, kV>(rr, M, M, P, sdY, ldP, sX, ldP,
                              [&](int i, int s_, float v) { sE[i * ldM + s_] = v; });
   __syncthreads();
+  // Hp and Gout are read: the next chunk's may come in
+  const int jn = j + static_cast<int>(gridDim.x);
+  ChunkPos qn{};
+  if (jn < total) {
+    qn = pos_of(jn);
+    fetch_state(jn);
+    cin = load_coefs<Tin>(p, qn);
+  }
 
   // ---------------------------------------------------------------- per token and token pair
   // per token (a warp each): wdot_t = sum over its rows of <W, X> (= <Gout, B~_t^T X_t>),
@@ -971,6 +1029,9 @@ __global__ void __launch_bounds__(kThreadsChunk, 1) bwd_chunk_kernel(const BwdPa
           fmaf(s_wx[s_], sW[s_ * ldP + pc], v);
   });
   __syncthreads();
+  // S and E are read: the next chunk's theta may come in
+  if (jn < total) issue_theta<Tin, kV>(p, sh, qn, s_th);
+  if constexpr (kV) cp_async_commit();
 
   // ---------------------------------------------------------------- rotation adjoint
   // the mask and fold parameters per token, a warp each, lanes over the other token (the last
@@ -1027,7 +1088,6 @@ __global__ void __launch_bounds__(kThreadsChunk, 1) bwd_chunk_kernel(const BwdPa
   // chunk-local suffix sums of d phi: this chunk's part of d theta, and the chunk's total.  The
   // tokens are split into G segments, one thread per (pair, segment): each segment's sum, then
   // every thread starts from the sum of the later segments and walks its tokens backwards.
-  const float* thraw = sm + L.th;
   {
     const int G = max(1, min(c, static_cast<int>(blockDim.x) / K)), per = (c + G - 1) / G;
     for (int e = threadIdx.x; e < K * G; e += blockDim.x) {
@@ -1038,13 +1098,23 @@ __global__ void __launch_bounds__(kThreadsChunk, 1) bwd_chunk_kernel(const BwdPa
     }
     __syncthreads();
     for (int e = threadIdx.x; e < K * G; e += blockDim.x) {
-      const int g = e / K, kk = e - g * K, t1 = min((g + 1) * per, q.nt);
+      const int g = e / K, kk = e - g * K, t1 = min((g + 1) * per, q.nt), tb = g * per;
       float v = 0.f;
       for (int h = G - 1; h > g; --h) v += s_red[h * K + kk];
-      for (int t = t1 - 1; t >= g * per; --t) {
-        v += sdphi[t * K + kk];
-        p.dtheta[(q.tok0 + static_cast<size_t>(t) * tstride) * K + kk] = s_dt[t] * v;
-        sdphi[t * K + kk] = v * theta_at<Tin, kV>(thraw, t * K + kk);  // theta . suffix, summed below
+      for (int ta = t1 - 1; ta >= tb; ta -= 4) {  // theta (from global) four tokens at a time
+        float th[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          th[u] = ta - u >= tb ? to_f(thg[(q.tok0 + static_cast<size_t>(ta - u) * tstride) * K + kk]) : 0.f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int t = ta - u;
+          if (t >= tb) {
+            v += sdphi[t * K + kk];
+            p.dtheta[(q.tok0 + static_cast<size_t>(t) * tstride) * K + kk] = s_dt[t] * v;
+            sdphi[t * K + kk] = v * th[u];  // theta . suffix, summed below
+          }
+        }
       }
       if (g == 0) p.wsSphi[slot * K + kk] = v;
     }
@@ -1080,6 +1150,9 @@ __global__ void __launch_bounds__(kThreadsChunk, 1) bwd_chunk_kernel(const BwdPa
     for (int o = 16; o > 0; o >>= 1) dadt += __shfl_xor_sync(0xffffffffu, dadt, o);
     if (t == 0) p.wsDa[slot] = dadt;
   }
+  __syncthreads();  // the next chunk's inputs overwrite this one's
+  }
+  if constexpr (kV) cp_async_wait_all();
 }
 
 // ------------------------------------------------------------------ carries across chunks
@@ -1237,7 +1310,10 @@ cudaError_t launch_chunk_kernels(const BwdParams& p, size_t bhn, cudaStream_t s)
   const size_t sm1 = static_cast<size_t>(local_smem(p.N, p.P, p.R, p.c, sizeof(Tin), sizeof(Tdy)).total) * 4;
   const size_t sm3 = static_cast<size_t>(chunk_smem(p.N, p.P, p.R, p.c, sizeof(Tin), sizeof(Tdy)).total) * 4;
   auto k1 = bwd_local_kernel<Tin, Tdy, kV, SN, SP, SR, SC>;
-  auto k3 = bwd_chunk_kernel<Tin, Tdy, kV, SN, SP, SR, SC>;
+  // 512 threads for the shapes specialised at compile time; 256 for the others, whose runtime
+  // dimensions need more registers than 512 threads leave (128 each)
+  constexpr int NT = SN ? kThreadsChunk : kThreads;
+  auto k3 = bwd_chunk_kernel<Tin, Tdy, kV, SN, SP, SR, SC, NT>;
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) != cudaSuccess)
     return e;
@@ -1249,7 +1325,12 @@ cudaError_t launch_chunk_kernels(const BwdParams& p, size_t bhn, cudaStream_t s)
   const long long total = static_cast<long long>(bhn) * p.K * p.P;
   bwd_scan_kernel<Tin><<<dim3(static_cast<unsigned>((total + kThreads - 1) / kThreads), 2), kThreads, 0, s>>>(p, total);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  k3<<<nblk, kThreadsChunk, sm3, s>>>(p);
+  // the adjoint kernel is persistent: one CTA per SM (its shared memory admits one)
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const unsigned grid3 = nblk < static_cast<unsigned>(sms) ? nblk : static_cast<unsigned>(sms);
+  k3<<<grid3, NT, sm3, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -1305,6 +1386,7 @@ cudaError_t launch_bwd(const BackwardArgs& a, cudaStream_t s) {
   p.M = w.c * d.R;
   p.nch = w.nch;
   p.K = d.N / 2;
+  p.BH = static_cast<int>(bhn);
   // 16-byte copies and tensor-core products: row lengths of 16 bytes' multiples, aligned operands,
   // (token, rank) rows a multiple of 16
   const bool vec = d.N % 16 == 0 && d.P % 8 == 0 && p.M % 16 == 0 && aligned16(a.x) && aligned16(a.B) &&
