@@ -209,7 +209,7 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
 }
 
 // The product of gemm() on the tensor cores: warp-level m16n8k8 TF32 MMAs in three passes per
-// fragment pair (split_tf32), accumulators in fp32 registers.  A warp computes a (16 MI) x
+// fragment pair (split_tf32), summed over k in fp32 registers.  A warp computes a (16 MI) x
 // (8 NJ) tile; fragments are read from shared memory with 32-bit loads in the MMA's register
 // layout (lane = 4 g + t: A rows g, g + 8, k t, t + 4; B k t, t + 4, column g; D rows g, g + 8,
 // columns 2 t, 2 t + 1).  With row strides of 4 (mod 32) words the loads along a k-contiguous
@@ -256,14 +256,21 @@ __device__ __forceinline__ void gemm_tc(int& rr, int NI, int NJd, int NK, const 
           split_tf32(B(k0 + t + 4, c), bh[nj][1], bl[nj][1]);
         }
       }
+      // each k-step's three passes into a fresh accumulator, added to the running sums by fp32
+      // adds: chained along k inside the MMA the sums drift low (measured on the MIMO
+      // rank-4 backward at T 4096: d theta 2.5e-4 of its RMS chained, 7.7e-5 this way, 8.2e-5
+      // with the CUDA-core product)
 #pragma unroll
       for (int mi = 0; mi < MI; ++mi)
 #pragma unroll
         for (int nj = 0; nj < NJ; ++nj)
           if (i0 + 16 * mi < NI && j0 + 8 * nj < NJd) {
-            mma_tf32(acc[mi][nj], al[mi], bh[nj]);
-            mma_tf32(acc[mi][nj], ah[mi], bl[nj]);
-            mma_tf32(acc[mi][nj], ah[mi], bh[nj]);
+            float part[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_tf32(part, al[mi], bh[nj]);
+            mma_tf32(part, ah[mi], bl[nj]);
+            mma_tf32(part, ah[mi], bh[nj]);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[mi][nj][r] += part[r];
           }
     }
 #pragma unroll

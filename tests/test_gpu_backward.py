@@ -102,3 +102,13 @@ def test_backward_full_size_sampled():
     sl = P.sample_slices(w.B, w.H, 2, 53)
     g, ref, sl = run(w.B, w.T, w.H, w.P, w.N, w.R, "bf16", w.seed, False, slices=sl)
     check(g, ref, sl, w.H, False)
+
+
+def test_backward_mimo_full_size_sampled():
+    """The MIMO rank-4 prefill shape (B8 T4096 H32 N64, 16-token chunks: 256 chunk scans per
+    sequence) through its compile-time-specialised kernels; sampled (b, h) sequences against the
+    oracle, with an entry state."""
+    w = synth.WORKLOADS["mimo-r4-prefill-bf16-b8-t4096-h32-p64-n64"]
+    sl = P.sample_slices(w.B, w.H, 2, 71)
+    g, ref, sl = run(w.B, w.T, w.H, w.P, w.N, w.R, "bf16", w.seed, True, slices=sl)
+    check(g, ref, sl, w.H, False)
