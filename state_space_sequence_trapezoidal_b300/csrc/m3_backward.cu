@@ -1,5 +1,6 @@
 // Backward pass of the prefill: gradients of y (and of the exit state h_T) with respect to
-// x, B, C, dt, A, lambda, theta and the entry state h, on CUDA cores in fp32.
+// x, B, C, dt, A, lambda, theta and the entry state h, in fp32 (the chunk products on the
+// tensor cores as three TF32 passes, the rest on CUDA cores).
 //
 // The forward map is the masked matrix form of Eq. (7) (section 2.3): within a chunk of c
 // tokens, with chunk-local log-decay sums l_i = sum_{s<=i} dt_s A, trapezoid column weights
@@ -38,8 +39,10 @@
 //                      reverse (Gout) over the chunks: Hp(k+1) = R(-sigma_k)(exp(l_last) Hp(k)
 //                      + dH(k)), Gout(k-1) = R(sigma_{k-1})(exp(l_last) Gout(k) + dG(k)), each
 //                      written over its chunk's dH / dG.
-//   bwd_chunk_kernel   one CTA per (batch row, head, chunk): the adjoint above, the mask and
-//                      fold parameters, the rotation adjoint, chunk-local suffix sums of d phi.
+//   bwd_chunk_kernel   persistent, one CTA per SM walking chunks (batch row, head, chunk): the
+//                      adjoint above, the mask and fold parameters, the rotation adjoint,
+//                      chunk-local suffix sums of d phi; the next chunk's theta, Hp, Gout and
+//                      coefficients are requested while the current one finishes.
 //   bwd_carry_kernel   one CTA per (batch row, head): suffix sums of d phi over chunks, the
 //                      per-(b, h) part of dA, the fold gradient of the sequence's first token.
 //   bwd_apply_kernel   one CTA per (batch row, head, chunk): adds the later chunks' d phi to
