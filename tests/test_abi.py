@@ -184,3 +184,27 @@ def test_backward_workspace_holds_the_chunk_states():
     # cotangent, N x P floats each
     assert n >= 2 * 8 * 32 * (4096 // 32) * 128 * 64 * 4
     assert lib.m3_ssm_prefill_backward_workspace(ctypes.byref(_dims(N=256, P=64))) == 256
+
+
+def test_backward_refuses_state_wider_than_1024():
+    lib = m3.load()
+    d = _dims(N=2048, P=4)  # N P = 8192 fits, but N / 2 pairs exceed the kernels' 512 threads
+    assert lib.m3_ssm_prefill_backward_workspace(ctypes.byref(d)) == 256
+    dd = _dims(N=2048, P=4)
+    assert lib.m3_ssm_prefill_backward(ctypes.byref(dd), 16, 16, 16, 16, 16, 16, 16, None, 16, None,
+                                       16, 16, 16, 16, 16, 16, 16, None, 16, 1 << 30, None) == SHAPE
+
+
+@pytest.mark.parametrize("R,c", [(1, 32), (2, 32), (4, 16), (8, 8)])
+def test_backward_chunk_length_per_rank(R, c):
+    """Chunks of 32 tokens while c R <= 64 (token, rank) rows, halved beyond: the workspace holds
+    two N x P fp32 states per chunk, plus per-chunk scalars and angle sums and one state per
+    sequence."""
+    lib = m3.load()
+    Bsz, T, H, N, P = 2, 1000, 3, 64, 64
+    d = _dims(B=Bsz, T=T, H=H, P=P, N=N, R=R)
+    n = lib.m3_ssm_prefill_backward_workspace(ctypes.byref(d))
+    bh, nch, K = Bsz * H, -(-T // c), N // 2
+    states = 2 * bh * nch * N * P * 4
+    rest = (bh * nch * (3 + 2 * K) + bh * N * P + bh) * 4 + 10 * 256
+    assert states <= n <= states + rest, (n, states, rest)
