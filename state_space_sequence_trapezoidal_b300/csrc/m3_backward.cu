@@ -191,17 +191,14 @@ __device__ __forceinline__ void gemm(int& rr, int NI, int NJ, int NK, const floa
 }
 
 // ------------------------------------------------------------------ tensor-core products
-// fp32 values as TF32 pairs: x = hi + lo with hi = x rounded to TF32 and lo the rest rounded
-// again; a product taken as a_lo b_hi + a_hi b_lo + a_hi b_hi (the lo lo term dropped) keeps
-// about 21 bits of each operand, the accuracy of an fp32 dot product for these sizes.
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
+// fp32 values as TF32 pairs: x = hi + lo with hi = x rounded to TF32's 10 mantissa bits (round
+// half away from zero, by integer adds and masks on the ALU rather than a conversion
+// instruction) and lo = x - hi, exact in fp32, of which the MMA reads the top 19 bits (TF32)
+// of its register.  A product taken as a_lo b_hi + a_hi b_lo + a_hi b_hi (the lo lo term
+// dropped) keeps about 21 bits of each operand, the accuracy of an fp32 dot product here.
 __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
-  hi = to_tf32(x);
-  lo = to_tf32(x - __uint_as_float(hi));
+  hi = (__float_as_uint(x) + 0x1000u) & 0xffffe000u;
+  lo = __float_as_uint(x - __uint_as_float(hi));
 }
 __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
   asm volatile(
