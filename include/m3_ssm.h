@@ -280,8 +280,9 @@ m3_status m3_ssd_decode_step(const m3_dims* dims, float* h, const void* x_t, con
  * reduction has a fixed order: results are bit-identical from run to run.  Supported when
  * N * P <= 8192, N even and N <= 1024; other shapes return M3_ERR_SHAPE.  Inputs, dtypes,
  * alignment and stream behaviour as m3_ssm_prefill; the workspace must hold
- * m3_ssm_prefill_backward_workspace bytes (its contents need no initialisation).
- * dims->chunk is ignored.
+ * m3_ssm_prefill_backward_workspace bytes (its contents need no initialisation); a bounded
+ * wait inside the kernels that ran out is recorded in the workspace's status word, read with
+ * m3_ssm_device_status(workspace) after the call (M3_ERR_TIMEOUT).  dims->chunk is ignored.
  */
 size_t m3_ssm_prefill_backward_workspace(const m3_dims* dims);
 

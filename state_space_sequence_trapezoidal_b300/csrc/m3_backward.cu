@@ -53,8 +53,12 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
+
+#include <cudaTypedefs.h>
 
 #include "m3_internal.h"
+#include "m3_ptx.cuh"
 
 namespace m3 {
 namespace {
@@ -70,6 +74,8 @@ constexpr int kMaxRows = 64;   // (token, rank) rows per chunk at most
 constexpr int kMaxTok = 32;    // tokens per chunk at most (one warp lane each)
 
 struct BwdParams {
+  CUtensorMap tmH;  // wsH as [BH nch N][P] fp32, box {32, N}, 128-byte swizzle (swizzled states only)
+  CUtensorMap tmG;  // wsG, the same
   const void* x;
   const void* B;
   const void* C;
@@ -99,6 +105,7 @@ struct BwdParams {
   float* wsDa;    // [BH][nch]       sum over chunk k's tokens of d(dt A) * dt
   float* wsDqf;   // [BH][nch]       d q of chunk k's first token through the fold
   float* dApart;  // [BH]
+  unsigned* status;  // device status word (a bounded wait that ran out: kDevTimeout)
   int T, H, N, P, R, c, M, nch, K;
   int BH;  // sequences (batch rows x heads)
 };
@@ -131,6 +138,19 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// A {32 columns, rows} box of a 2-D fp32 tensor map into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+// Float offset of state entry (n, p) in a state of `rows` rows stored by tma_load_2d with the
+// 128-byte swizzle: 32-column boxes of rows x 128 B, the 16-byte group of p within its 128-byte
+// row turned by n mod 8 (the destination is 1024-byte aligned).
+__device__ __forceinline__ int swz(int n, int p, int rows) {
+  return (p >> 5) * (rows * 32) + n * 32 + ((((p & 31) >> 2) ^ (n & 7)) << 2) + (p & 3);
+}
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Register-tiled product on the CUDA cores, for the shapes the tensor-core product below does
@@ -216,7 +236,7 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
 // operand are free of bank conflicts (4 g + t); along an index-contiguous one two lanes share
 // a bank.  Needs NI % 16 == 0, NJ % 8 == 0 and NK % 8 == 0 (fragments wholly in or out); the
 // in / out tests are the same for all lanes of a warp, as mma.sync requires.
-template <int MI, int NJ, bool kAK, bool kBK, typename FO>
+template <int MI, int NJ, bool kAK, bool kBK, bool kSwzB, typename FO>
 __device__ __forceinline__ void gemm_tc(int& rr, int NI, int NJd, int NK, const float* __restrict__ a,
                                         int lda, const float* __restrict__ b, int ldb, FO out) {
   constexpr int WI = 16 * MI, WJ = 8 * NJ;
@@ -227,7 +247,14 @@ __device__ __forceinline__ void gemm_tc(int& rr, int NI, int NJd, int NK, const 
   if (w < 0) w += nw;
   rr += ntile;
   auto A = [&](int i, int k) { return kAK ? a[i * lda + k] : a[k * lda + i]; };
-  auto B = [&](int k, int j) { return kBK ? b[j * ldb + k] : b[k * ldb + j]; };
+  // kSwzB: b is a state in the swizzled layout of swz() with ldb rows; B(k, j) = state(j, k) when
+  // kBK, else state(k, j)
+  auto B = [&](int k, int j) {
+    if constexpr (kSwzB)
+      return kBK ? b[swz(j, k, ldb)] : b[swz(k, j, ldb)];
+    else
+      return kBK ? b[j * ldb + k] : b[k * ldb + j];
+  };
   for (int tile = w; tile < ntile; tile += nw) {
     const int i0 = (tile / nwj) * WI, j0 = (tile % nwj) * WJ;
     float acc[MI][NJ][4];
@@ -293,7 +320,7 @@ template <int MI, int NJ, int TI, int TJ, bool kAK, bool kBK, bool kV, typename 
 __device__ __forceinline__ void product(int& rr, int NI, int NJd, int NK, const float* __restrict__ a,
                                         int lda, const float* __restrict__ b, int ldb, FO out) {
   if constexpr (kV)
-    gemm_tc<MI, NJ, kAK, kBK>(rr, NI, NJd, NK, a, lda, b, ldb, out);
+    gemm_tc<MI, NJ, kAK, kBK, false>(rr, NI, NJd, NK, a, lda, b, ldb, out);
   else
     gemm<TI, TJ, kAK, kBK>(rr, NI, NJd, NK, a, lda, b, ldb, out);
 }
@@ -390,9 +417,12 @@ __host__ __device__ inline LocalSmem local_smem(int N, int P, int R, int c, int 
 
 struct ChunkSmem {
   InSmem in;
-  int Q, XG, W, Hp, Go, S, E, th, dphi, Mh, ex, dM, dexp, wdot, dell, dgam, dq, red, total;
+  int Q, XG, W, Hp, Go, S, E, th, dphi, Mh, ex, dM, dexp, wdot, dell, dgam, dq, red, bar, total;
 };
-__host__ __device__ inline ChunkSmem chunk_smem(int N, int P, int R, int c, int szIn, int szDy) {
+// swz_state: Hp and Gout dense in the swizzled layout of swz(), each at a 1024-byte boundary of
+// a base that the kernel aligns to 1024 bytes; else rows padded to P + kPad.
+__host__ __device__ inline ChunkSmem chunk_smem(int N, int P, int R, int c, int szIn, int szDy,
+                                                bool swz_state = false) {
   const int K = N / 2, M = c * R;
   ChunkSmem s{};
   Carve cv;
@@ -402,8 +432,9 @@ __host__ __device__ inline ChunkSmem chunk_smem(int N, int P, int R, int c, int 
   const int raw = raw_total(N, P, R, c, szIn, szDy);
   carve_inputs(cv, s.in, N, P, R, c, szIn, szDy, raw <= 2 * M * (N + kPad) ? s.Q : -1, kPad, false);
   s.W = cv.take(M * (P + kPad));   // B~ Gout; then d phi per (token, pair), where it fits
-  s.Hp = cv.take(N * (P + kPad));  // Hp; the next chunk's from the end of the first products
-  s.Go = cv.take(N * (P + kPad));  // Gout, likewise
+  if (swz_state) cv.o = (cv.o + 255) & ~255;
+  s.Hp = cv.take(N * (swz_state ? P : P + kPad));  // Hp; the next chunk's from the end of the first products
+  s.Go = cv.take(N * (swz_state ? P : P + kPad));  // Gout, likewise
   s.S = cv.take(M * (M + kPad));   // C~ B~^T, then Mh o S; then the next chunk's theta
   s.E = cv.take(M * (M + kPad));   // dY X^T, then Mh o E
   s.th = c * K <= 2 * M * (M + kPad) ? s.S : cv.take(c * K);  // theta, fp32 or raw 16-bit
@@ -417,6 +448,7 @@ __host__ __device__ inline ChunkSmem chunk_smem(int N, int P, int R, int c, int 
   s.dgam = cv.take(c);
   s.dq = cv.take(c);
   s.red = cv.take(kThreadsChunk);
+  s.bar = cv.take(4);  // mbarrier of the swizzled state copies
   s.total = cv.o;
   return s;
 }
@@ -831,13 +863,17 @@ __global__ void __launch_bounds__(kThreads) bwd_scan_kernel(const BwdParams p, l
 }
 
 // ------------------------------------------------------------------ per-chunk adjoint
-template <typename Tin, typename Tdy, bool kV, int SN, int SP, int SR, int SC, int NT>
-__global__ void __launch_bounds__(NT, 1) bwd_chunk_kernel(const BwdParams p) {
-  extern __shared__ __align__(16) float sm[];
+// kTS: Hp and Gout arrive by TMA tensor copies (p.tmH, p.tmG) in the swizzled layout of swz(),
+// completing on an mbarrier, instead of 16-byte thread copies into padded rows (P % 32 == 0).
+template <typename Tin, typename Tdy, bool kV, int SN, int SP, int SR, int SC, int NT, bool kTS>
+__global__ void __launch_bounds__(NT, 1) bwd_chunk_kernel(const __grid_constant__ BwdParams p) {
+  extern __shared__ __align__(16) float sm_raw[];
+  // the base at a 1024-byte boundary (the swizzled copies' destinations need it)
+  float* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u) / 4u;
   const Shape sh = shape_of<SN, SP, SR, SC>(p);
   const int N = sh.N, P = sh.P, R = sh.R, c = sh.c, M = sh.M, K = sh.K, NP = N * P;
   const int ldN = N + kPad, ldP = P + kPad, ldM = M + kPad, ldT = c + 1;  // = L.ldN, L.ldP
-  const ChunkSmem S = chunk_smem(N, P, R, c, sizeof(Tin), sizeof(Tdy));
+  const ChunkSmem S = chunk_smem(N, P, R, c, sizeof(Tin), sizeof(Tdy), kTS);
   const InSmem& L = S.in;
   const size_t tstride = p.H;
   const int total = p.BH * p.nch;
@@ -876,10 +912,19 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_kernel(const BwdParams p) {
   const Tin* thg = static_cast<const Tin*>(p.theta);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   // a chunk's Hp and Gout into their areas (asynchronous copies when kV)
+  const uint32_t s_bar = smem_u32(sm + S.bar);
   auto fetch_state = [&](size_t slot_) {
     const float* hp = p.wsH + slot_ * NP;
     const float* go = p.wsG + slot_ * NP;
-    if constexpr (kV) {
+    if constexpr (kTS) {
+      if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(s_bar, 2u * static_cast<uint32_t>(NP) * 4u);
+        for (int bx = 0; bx < P / 32; ++bx) {
+          tma_load_2d(smem_u32(sHp + bx * N * 32), &p.tmH, s_bar, 32 * bx, static_cast<int>(slot_) * N);
+          tma_load_2d(smem_u32(sGo + bx * N * 32), &p.tmG, s_bar, 32 * bx, static_cast<int>(slot_) * N);
+        }
+      }
+    } else if constexpr (kV) {
       const int per = P / 4;
       for (int e = threadIdx.x; e < N * per; e += blockDim.x) {
         const int n = e / per, col = (e - n * per) * 4;
@@ -899,6 +944,13 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_kernel(const BwdParams p) {
   // Persistent: CTA b takes chunks b, b + gridDim.x, ...; theta, Hp, Gout, dt and lambda of the
   // next chunk are requested while the current one finishes (their areas are free by then).
   CoefIn cin{0.f, 0.f, 0.f, 0.f, 0.f};
+  if constexpr (kTS) {
+    if (threadIdx.x == 0) {
+      mbar_init(s_bar, 1);
+      fence_mbar_init();
+    }
+    __syncthreads();
+  }
   if (static_cast<int>(blockIdx.x) < total) {
     const ChunkPos q0 = pos_of(blockIdx.x);
     issue_theta<Tin, kV>(p, sh, q0, s_th);
@@ -906,7 +958,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_kernel(const BwdParams p) {
     if constexpr (kV) cp_async_commit();
     cin = load_coefs<Tin>(p, q0);
   }
-  for (int j = blockIdx.x; j < total; j += gridDim.x) {
+  for (int j = blockIdx.x, it = 0; j < total; j += gridDim.x, ++it) {
   const ChunkPos q = pos_of(j);
   const size_t slot = j;
   const float A = cin.A;  // (warp 0 only: the coefficients and d dt use it)
@@ -918,8 +970,16 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_kernel(const BwdParams p) {
   issue_rows<Tdy, kV>(static_cast<const Tdy*>(p.dy), q, tstride, c, R, P, sdY, ldP, reinterpret_cast<Tdy*>(sm + L.rY));
   if constexpr (kV) cp_async_commit();
   chunk_coefs_from(sh, q, A, L, sm, cin);
-  if constexpr (kV) asm volatile("cp.async.wait_group 1;" ::: "memory");  // theta, Hp, Gout
-  __syncthreads();
+  if constexpr (kV) asm volatile("cp.async.wait_group 1;" ::: "memory");  // theta (and Hp, Gout)
+  if constexpr (kTS) {
+    // Hp and Gout: a wait that runs out (bounded) ends the CTA's work and is reported
+    if (!__syncthreads_and(mbar_wait(s_bar, static_cast<uint32_t>(it) & 1u))) {
+      if (threadIdx.x == 0) atomicOr(p.status, kDevTimeout);
+      break;
+    }
+  } else {
+    __syncthreads();
+  }
   chunk_angles<Tin, kV>(q, sh, sm, L, s_th, nullptr);
   row_weights(q, c, R, L, sm);
   if constexpr (kV) cp_async_wait_all();
@@ -942,27 +1002,34 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_kernel(const BwdParams p) {
     s_ex[ti * ldT + ts] = ex;
     s_Mh[ti * ldT + ts] = m;
   }
-  {  // <Gout, Hp>, one partial per thread
+  {  // <Gout, Hp>, one partial per thread (both states in the same layout)
     float gh = 0.f;
     for (int e = threadIdx.x; e < NP; e += blockDim.x) {
       const int n = e / P, col = e - n * P;
-      gh = fmaf(sGo[n * ldP + col], sHp[n * ldP + col], gh);
+      const int o = kTS ? e : n * ldP + col;
+      gh = fmaf(sGo[o], sHp[o], gh);
     }
     s_red[threadIdx.x] = gh;
   }
   int rr = 0;
   // W = B~ Gout, S = C~ B~^T, Q = dY Hp^T, XG = X Gout^T, E = dY X^T (tiles of about equal
   // work, the largest products first)
-  product<2, 2, 2, 4, true, false, kV>(rr, M, P, N, sBt, ldN, sGo, ldP,
-                              [&](int s_, int pc, float v) { sW[s_ * ldP + pc] = v; });
+  auto state_product = [&](auto kbk, int NJd, int NK, const float* a, int lda, const float* st, auto out) {
+    constexpr bool kBK = decltype(kbk)::value;
+    if constexpr (kTS)
+      gemm_tc<2, kBK ? 2 : 2, true, kBK, true>(rr, M, NJd, NK, a, lda, st, N, out);
+    else
+      product<2, 2, kBK ? 4 : 2, 4, true, kBK, kV>(rr, M, NJd, NK, a, lda, st, ldP, out);
+  };
+  state_product(std::false_type{}, P, N, sBt, ldN, sGo,
+                [&](int s_, int pc, float v) { sW[s_ * ldP + pc] = v; });
   product<2, 2, 2, 4, true, true, kV>(rr, M, M, N, sCt, ldN, sBt, ldN,
                              [&](int i, int s_, float v) { sS[i * ldM + s_] = v; });
-  product<2, 2, 4, 4, true, true, kV>(rr, M, N, P, sdY, ldP, sHp, ldP,
-                             [&](int i, int n, float v) { sQ[i * ldN + n] = v; });
-  product<2, 2, 4, 4, true, true, kV>(rr, M, N, P, sX, ldP, sGo, ldP,
-                             [&](int s_, int n, float v) { sXG[s_ * ldN + n] = v; });
+  state_product(std::true_type{}, N, P, sdY, ldP, sHp, [&](int i, int n, float v) { sQ[i * ldN + n] = v; });
+  state_product(std::true_type{}, N, P, sX, ldP, sGo, [&](int s_, int n, float v) { sXG[s_ * ldN + n] = v; });
   product<2, 2, 2, 4, true, true, kV>(rr, M, M, P, sdY, ldP, sX, ldP,
                              [&](int i, int s_, float v) { sE[i * ldM + s_] = v; });
+  if constexpr (kTS) fence_proxy_async_smem();  // the reads of Hp and Gout before the TMA rewrites them
   __syncthreads();
   // Hp and Gout are read: the next chunk's may come in
   const int jn = j + static_cast<int>(gridDim.x);
@@ -1303,7 +1370,7 @@ int plan_c(const m3_dims& d) {
   const int si = dtype_bytes(d.in_dtype), sy = dtype_bytes(d.out_dtype);
   for (int c = kMaxTok; c >= 1; c /= 2) {
     if (c * d.R > kMaxRows) continue;
-    if (static_cast<size_t>(chunk_smem(d.N, d.P, d.R, c, si, sy).total) * 4 <= kSmemLimit &&
+    if (static_cast<size_t>(chunk_smem(d.N, d.P, d.R, c, si, sy).total) * 4 + 1024 <= kSmemLimit &&
         static_cast<size_t>(local_smem(d.N, d.P, d.R, c, si, sy).total) * 4 <= kSmemLimit)
       return c;
   }
@@ -1312,15 +1379,44 @@ int plan_c(const m3_dims& d) {
 
 bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-template <typename Tin, typename Tdy, bool kV, int SN, int SP, int SR, int SC>
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// A chunk-state array [rows][P] fp32 as a 2-D tensor map with boxes of {32 columns, N rows} and
+// the 128-byte swizzle (32 fp32 columns are exactly 128 bytes).
+bool state_map(CUtensorMap* m, float* base, size_t rows, int P, int N) {
+  auto fn = tmap_encoder();
+  if (!fn || P % 32 != 0 || N > 256) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(P), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(P) * 4};
+  const cuuint32_t box[2] = {32u, static_cast<cuuint32_t>(N)};
+  const cuuint32_t es[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename Tin, typename Tdy, bool kV, int SN, int SP, int SR, int SC, bool kTS = false>
 cudaError_t launch_chunk_kernels(const BwdParams& p, size_t bhn, cudaStream_t s) {
   const size_t sm1 = static_cast<size_t>(local_smem(p.N, p.P, p.R, p.c, sizeof(Tin), sizeof(Tdy)).total) * 4;
-  const size_t sm3 = static_cast<size_t>(chunk_smem(p.N, p.P, p.R, p.c, sizeof(Tin), sizeof(Tdy)).total) * 4;
+  // (+ 1024: the adjoint kernel aligns its base to 1024 bytes)
+  const size_t sm3 =
+      static_cast<size_t>(chunk_smem(p.N, p.P, p.R, p.c, sizeof(Tin), sizeof(Tdy), kTS).total) * 4 + 1024;
   auto k1 = bwd_local_kernel<Tin, Tdy, kV, SN, SP, SR, SC>;
   // 512 threads for the shapes specialised at compile time; 256 for the others, whose runtime
   // dimensions need more registers than 512 threads leave (128 each)
   constexpr int NT = SN ? kThreadsChunk : kThreads;
-  auto k3 = bwd_chunk_kernel<Tin, Tdy, kV, SN, SP, SR, SC, NT>;
+  auto k3 = bwd_chunk_kernel<Tin, Tdy, kV, SN, SP, SR, SC, NT, kTS>;
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1)) != cudaSuccess)
     return e;
@@ -1384,6 +1480,7 @@ cudaError_t launch_bwd(const BackwardArgs& a, cudaStream_t s) {
   p.wsDa = reinterpret_cast<float*>(a.ws + w.off_da_chunk);
   p.wsDqf = reinterpret_cast<float*>(a.ws + w.off_dqf);
   p.dApart = reinterpret_cast<float*>(a.ws + w.off_da);
+  p.status = reinterpret_cast<unsigned*>(a.ws);  // the status word at the workspace start
   p.T = d.T;
   p.H = d.H;
   p.N = d.N;
@@ -1394,12 +1491,22 @@ cudaError_t launch_bwd(const BackwardArgs& a, cudaStream_t s) {
   p.nch = w.nch;
   p.K = d.N / 2;
   p.BH = static_cast<int>(bhn);
+  // the call's device status starts clear (m3_ssm_device_status reads it)
+  if ((e = cudaMemsetAsync(a.ws, 0, sizeof(unsigned), s)) != cudaSuccess) return e;
   // 16-byte copies and tensor-core products: row lengths of 16 bytes' multiples, aligned operands,
   // (token, rank) rows a multiple of 16
   const bool vec = d.N % 16 == 0 && d.P % 8 == 0 && p.M % 16 == 0 && aligned16(a.x) && aligned16(a.B) &&
                    aligned16(a.C) && aligned16(a.theta) && aligned16(a.dy);
   // shapes with kernels specialised at compile time: SISO N 128 P 64 and MIMO rank 4 N 64 P 64
-  if (vec && d.N == 128 && d.P == 64 && d.R == 1 && w.c == 32)
+  // for them, the chunk states go by TMA tensor copies when the maps can be made
+  const size_t srows = bhn * static_cast<size_t>(w.nch) * d.N;
+  const bool tmaps = vec && srows < (size_t(1) << 31) && state_map(&p.tmH, p.wsH, srows, d.P, d.N) &&
+                     state_map(&p.tmG, p.wsG, srows, d.P, d.N);
+  if (tmaps && d.N == 128 && d.P == 64 && d.R == 1 && w.c == 32)
+    e = launch_chunk_kernels<Tin, Tdy, true, 128, 64, 1, 32, true>(p, bhn, s);
+  else if (tmaps && d.N == 64 && d.P == 64 && d.R == 4 && w.c == 16)
+    e = launch_chunk_kernels<Tin, Tdy, true, 64, 64, 4, 16, true>(p, bhn, s);
+  else if (vec && d.N == 128 && d.P == 64 && d.R == 1 && w.c == 32)
     e = launch_chunk_kernels<Tin, Tdy, true, 128, 64, 1, 32>(p, bhn, s);
   else if (vec && d.N == 64 && d.P == 64 && d.R == 4 && w.c == 16)
     e = launch_chunk_kernels<Tin, Tdy, true, 64, 64, 4, 16>(p, bhn, s);
